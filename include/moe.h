@@ -1,0 +1,236 @@
+/*
+ * moe.h -- C ABI of the B300 (sm_103a) DeepSeekMoE feed-forward layer.
+ *
+ * The layer (DeepSeek-V3 technical report; ai.flicky.cc "06 - DeepSeek-V3
+ * reading" section 2.1.2 and xyznot.com "DeepSeek-V3 technical report"
+ * Method 2):
+ *
+ *   h'_t    = u_t + sum_{s<N_s} FFN^(s)_s(u_t) + sum_{i<N_r} g_{i,t} FFN^(r)_i(u_t)
+ *   s_{i,t} = sigmoid(u_t^T e_i)
+ *   g'_{i,t}= s_{i,t} if s_{i,t} + b_i is among the K_r largest of {s_{j,t} + b_j}, else 0
+ *   g_{i,t} = g'_{i,t} / sum_j g'_{j,t}
+ *   FFN(x)  = W2 (SiLU(W1 x) * (W3 x))       (SwiGLU expert of three d x I matrices)
+ *
+ * and the auxiliary-loss-free bias update between steps (same section):
+ * b_i decreases by gamma when expert i is overloaded, increases when it is
+ * underloaded.  FP8 variant (ai.flicky.cc section 3.3): E4M3 operands for the
+ * expert GEMMs, activations scaled per 1 x 128 tile, weights per 128 x 128
+ * block, partial sums promoted to FP32 every 128 elements of K; the router
+ * stays bf16 with fp32 accumulation.
+ *
+ * Conventions shared by every call
+ *   Memory     Every pointer is DEVICE memory owned by the caller, unless a
+ *              parameter says otherwise.  The library allocates nothing and
+ *              keeps no mutable global state; each call only enqueues work.
+ *              Base pointers must be 16-byte aligned.
+ *   Streams    `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *              default stream).  Calls are asynchronous on that stream.
+ *   bf16       bf16 tensors are passed as uint16_t bit patterns.
+ *   Layouts    Row-major.  Weights are K-major (nn.Linear: [out, in]).
+ *   Errors     Argument and shape errors are returned at once and enqueue
+ *              nothing.  Errors found on the device (an out-of-range expert
+ *              index, a bounded wait that ran out) are written to a status
+ *              word at the start of the workspace; moe_read_device_status()
+ *              returns it.  Every call that takes a workspace clears that word
+ *              first, so it reports the most recent such call.
+ *   Limits     1 <= k <= min(E, 32); E <= 1024; d and I multiples of 128;
+ *              T >= 0 (T == 0 enqueues nothing and succeeds).
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null pointer, bad shape, k > E, misaligned pointer */
+  MOE_ERR_UNSUPPORTED = 2,  /* shape outside the limits above */
+  MOE_ERR_WORKSPACE = 3,    /* workspace smaller than moe_workspace_size() */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, attribute, ...) */
+  MOE_ERR_TIMEOUT = 5,      /* device: a bounded wait inside a kernel ran out */
+  MOE_ERR_BAD_INDEX = 6     /* device: an expert index outside [0, E) */
+} moe_status;
+
+typedef enum { MOE_BF16 = 0, MOE_FP8_E4M3 = 1 } moe_precision;
+
+/* Layer shape.  T tokens, hidden size d, E routed experts, k of them per
+ * token, n_shared shared experts, SwiGLU intermediate size inter (= I) of
+ * every expert, prec the precision of the expert GEMMs. */
+typedef struct {
+  int32_t T, d, E, k, n_shared, inter;
+  int32_t prec; /* moe_precision */
+} moe_dims;
+
+/*
+ * Expert weights of one layer.
+ *   w13  routed gate/up weights [E, 2I, d]: for j = 0 .. I/128-1, rows
+ *        [256j, 256j+128) are W1 rows [128j, 128j+128) and rows
+ *        [256j+128, 256j+256) are W3 rows [128j, 128j+128).  (One 256-row
+ *        tile then holds matching gate and up features; moe_pack_gate_up
+ *        builds this layout.)  bf16, or E4M3 bytes when prec is FP8.
+ *   w2   routed down weights [E, d, I].
+ *   w13_scale, w2_scale  FP8 only: fp32 scale of every 128 x 128 block,
+ *        [E, 2I/128, d/128] and [E, d/128, I/128]; NULL for bf16.
+ *   ws13, ws2, ws13_scale, ws2_scale  the same for the n_shared shared experts.
+ *   centroids  router centroids e_i, [E, d] bf16 (the router is never FP8).
+ */
+typedef struct {
+  const void* w13;
+  const float* w13_scale;
+  const void* w2;
+  const float* w2_scale;
+  const void* ws13;
+  const float* ws13_scale;
+  const void* ws2;
+  const float* ws2_scale;
+  const uint16_t* centroids;
+} moe_weights;
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(moe_status s);
+
+/* Bytes of workspace moe_forward (and every call below that takes `ws`) needs
+ * for these dimensions.  The workspace is caller-owned device memory, 256-byte
+ * aligned, with no required initial content. */
+moe_status moe_workspace_size(const moe_dims* dims, size_t* bytes);
+
+/*
+ * Router: s = sigmoid(u e^T), top-k of s + b, gates normalised over the
+ * selected unbiased affinities (ai.flicky.cc 2.1.2, the s_{i,t} and g'_{i,t}
+ * equations; xyznot.com Method 2, the normalisation of g').
+ *   u          [T, d] bf16 layer input.
+ *   centroids  [E, d] bf16.
+ *   bias       [E] fp32 selection bias (read only).
+ *   topk_idx   out [T, k] int32: the selected experts of each token, by biased
+ *              score descending (exact ties: lower index first).
+ *   topk_gate  out [T, k] fp32: g of each selected expert (sums to 1 per token).
+ *   counts     out [E] int32: tokens routed to each expert (the load).
+ * Logits are a bf16 x bf16 -> fp32 tensor-core GEMM.  A NaN score ranks
+ * below every number.
+ */
+moe_status moe_route(const moe_dims* dims, const uint16_t* u, const uint16_t* centroids,
+                     const float* bias, int32_t* topk_idx, float* topk_gate, int32_t* counts,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Dropless dispatch (ai.flicky.cc 2.1.2: no token is dropped): groups the
+ * T*k (token, expert) pairs by expert, tokens ascending within an expert.
+ *   topk_idx  [T, k] int32 (as from moe_route); entries outside [0, E) raise
+ *             MOE_ERR_BAD_INDEX on the device and are skipped.
+ *   u         [T, d] bf16.
+ *   offsets   out [E+1] int32: rows of expert e are [offsets[e], offsets[e+1]).
+ *   perm      out [T*k] int32: token of every permuted row.
+ *   slot      out [T, k] int32: permuted row of pair (t, j).
+ *   x_perm    out [T*k, d]: x_perm[r] = u[perm[r]] as bf16, or (FP8) as E4M3
+ *             codes of u quantised per 1 x 128 tile.
+ *   x_scale   FP8: out [d/128, T*k] fp32 tile scales (amax/448, column-major
+ *             by row so a 128-row tile's scales are contiguous); NULL for bf16.
+ */
+moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, const uint16_t* u,
+                       int32_t* offsets, int32_t* perm, int32_t* slot, void* x_perm, float* x_scale,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Grouped SwiGLU experts: for g < n_groups, rows [offsets[g], offsets[g+1])
+ * of x go through expert g: y = W2_g (SiLU(W1_g x) * (W3_g x)).
+ *   rows      rows allocated in x and y (offsets[n_groups] <= rows).
+ *   offsets   [n_groups+1] int32 device array, non-decreasing, offsets[0] = 0.
+ *   x         [rows, d] bf16, or E4M3 codes with x_scale [d/128, rows] fp32.
+ *   w13, w2   weights of the n_groups experts in the moe_weights layout
+ *             (with their block scales for FP8).
+ *   y         out [rows, d] bf16.
+ * The gate/up product and SiLU(g)*u are one fused tcgen05 GEMM; FP8 also
+ * quantises h per 1 x 128 tile inside that GEMM before the down product.
+ */
+moe_status moe_grouped_ffn(const moe_dims* dims, int32_t n_groups, int32_t rows, const int32_t* offsets,
+                           const void* x, const float* x_scale, const void* w13, const float* w13_scale,
+                           const void* w2, const float* w2_scale, uint16_t* y, void* ws,
+                           size_t ws_bytes, void* stream);
+
+/*
+ * Combine (the layer equation of ai.flicky.cc 2.1.2):
+ *   out_t = u_t + sum_{s<N_s} shared_y[s, t] + sum_{j<k} topk_gate[t, j] * y_perm[slot[t, j]]
+ * summed in fp32 in that order, rounded once to bf16.
+ *   shared_y  [n_shared, T, d] bf16, or NULL when n_shared == 0.
+ *   y_perm    [T*k, d] bf16;  slot [T, k] int32;  topk_gate [T, k] fp32.
+ *   out       out [T, d] bf16.
+ * A slot outside [0, T*k) contributes nothing (its term is skipped).
+ */
+moe_status moe_combine(const moe_dims* dims, const uint16_t* u, const uint16_t* shared_y,
+                       const uint16_t* y_perm, const int32_t* slot, const float* topk_gate,
+                       uint16_t* out, void* stream);
+
+/*
+ * Auxiliary-loss-free bias update (ai.flicky.cc 2.1.2; xyznot.com Method 2,
+ * gamma = 0.001): in fp32, b_i <- b_i + gamma * sign(T*k/E - counts_i), so an
+ * overloaded expert loses gamma, an underloaded one gains gamma, and one
+ * exactly at the mean load keeps its bias.
+ *   counts  [E] int32 loads of the step;  bias  [E] fp32, updated in place.
+ */
+moe_status moe_bias_update(int32_t E, int32_t T, int32_t k, const int32_t* counts, float gamma,
+                           float* bias, void* stream);
+
+/*
+ * The whole layer: route, dispatch, routed and shared SwiGLU experts,
+ * combine.  bias is read only (moe_bias_update is its only writer).
+ *   u           [T, d] bf16.
+ *   out         out [T, d] bf16 (h').
+ *   counts_out  out [E] int32 per-expert loads of this step, or NULL.
+ * The call enqueues its kernels and returns; it never waits on the device.
+ */
+moe_status moe_forward(const moe_dims* dims, const moe_weights* w, const uint16_t* u, const float* bias,
+                       uint16_t* out, int32_t* counts_out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_forward with stage timing.  `events` holds n_events >= MOE_PROFILE_EVENTS
+ * cudaEvent_t handles (passed as void*) created by the caller; the call
+ * records events[0] on `stream` before its first kernel and events[i] after
+ * stage i: 1 router logits GEMM, 2 top-k, 3 expert scan + tile plan,
+ * 4 row gather (and FP8 quantisation), 5 routed gate/up + SwiGLU GEMM,
+ * 6 routed down GEMM, 7 shared gate/up GEMM, 8 shared down GEMM, 9 combine
+ * (stages 7 and 8 are empty when n_shared == 0).  The device work is that of
+ * moe_forward.
+ */
+#define MOE_PROFILE_EVENTS 10
+moe_status moe_forward_profiled(const moe_dims* dims, const moe_weights* w, const uint16_t* u, const float* bias,
+                                uint16_t* out, int32_t* counts_out, void* ws, size_t ws_bytes, void* stream,
+                                void* const* events, int32_t n_events);
+
+/*
+ * Offline weight preparation (not part of the timed layer).
+ * moe_pack_gate_up: w13[e] = interleave of w1[e], w3[e] ([E, I, d] bf16 each)
+ *   in 128-row blocks, the layout moe_weights.w13 describes.
+ * moe_quantize_fp8_blocks: w [rows, cols] bf16 -> q [rows, cols] E4M3 codes and
+ *   scale [rows/128, cols/128] fp32 with scale = amax/448 of each 128 x 128 block
+ *   (1 for an all-zero block), q = round-to-nearest-even, saturating, of w/scale
+ *   (ai.flicky.cc 3.3 item 2).  rows and cols multiples of 128.
+ */
+moe_status moe_pack_gate_up(const uint16_t* w1, const uint16_t* w3, int32_t E, int32_t inter, int32_t d,
+                            uint16_t* w13, void* stream);
+moe_status moe_quantize_fp8_blocks(const uint16_t* w, int64_t rows, int32_t cols, uint8_t* q, float* scale,
+                                   void* stream);
+
+/* Synchronises `stream` and returns the device status word of workspace `ws`
+ * (MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_BAD_INDEX), or MOE_ERR_CUDA if the stream
+ * itself reports an error. */
+moe_status moe_read_device_status(const void* ws, void* stream);
+
+/*
+ * Self-test of the bounded waits: launches one CTA that waits on an mbarrier
+ * nothing ever arrives on, with a limit of timeout_us microseconds.  The
+ * kernel then gives up, records MOE_ERR_TIMEOUT in the status word of `ws`
+ * and returns normally, leaving the context usable.  Every wait inside the
+ * library's kernels is bounded the same way (with a limit of seconds).
+ */
+moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, int32_t timeout_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

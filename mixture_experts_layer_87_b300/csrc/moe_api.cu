@@ -1,0 +1,536 @@
+// C ABI of the B300 DeepSeekMoE layer (declarations and contracts: moe.h).
+//
+// Host side only marshals: it validates arguments, lays out the workspace,
+// encodes TMA tensor maps and enqueues kernels on the caller's stream.  It
+// never allocates device memory, never synchronises (except
+// moe_read_device_status, whose job that is) and never reads device data.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <cstring>
+
+#include "kernels.cuh"
+#include "moe.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+// Byte offsets of every buffer inside the caller's workspace.
+struct Layout {
+  size_t status, z, idx, gate, counts, mask, wprefix, cnt, offsets, groups, mt_total, perm, slot;
+  size_t x, xs, uq, uqs, h, hs, hsh, hshs, y, ysh, total;
+};
+
+Layout make_layout(const moe_dims& d) {
+  Layout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes > 0 ? bytes : 1);
+    return o;
+  };
+  const int64_t T = d.T, R = T * d.k, W = (T + 31) / 32, E = d.E, I = d.inter, D = d.d, Ns = d.n_shared;
+  const bool fp8 = d.prec == MOE_FP8_E4M3;
+  const int64_t eb = fp8 ? 1 : 2;  // bytes per GEMM operand element
+  L.status = take(256);
+  L.z = take(T * E * 4);
+  L.idx = take(R * 4);
+  L.gate = take(R * 4);
+  L.counts = take(E * 4);
+  L.mask = take(E * W * 4);
+  L.wprefix = take(E * W * 4);
+  L.cnt = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.groups = take((E + Ns + 1) * sizeof(GroupEntry));
+  L.mt_total = take(16);
+  L.perm = take(R * 4);
+  L.slot = take(R * 4);
+  L.x = take(R * D * eb);
+  L.xs = fp8 ? take(D / 128 * R * 4) : 0;
+  L.uq = fp8 ? take(T * D) : 0;
+  L.uqs = fp8 ? take(D / 128 * T * 4) : 0;
+  L.h = take(R * I * eb);
+  L.hs = fp8 ? take(I / 128 * R * 4) : 0;
+  L.hsh = take(Ns * T * I * eb);
+  L.hshs = fp8 ? take(I / 128 * Ns * T * 4) : 0;
+  L.y = take(R * D * 2);
+  L.ysh = take(Ns * T * D * 2);
+  L.total = off;
+  return L;
+}
+
+template <class P>
+P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(static_cast<uint8_t*>(ws) + off);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_dims(const moe_dims* d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->T < 0 || d->d <= 0 || d->E <= 0 || d->k <= 0 || d->n_shared < 0 || d->inter <= 0) return MOE_ERR_INVALID_ARG;
+  if (d->prec != MOE_BF16 && d->prec != MOE_FP8_E4M3) return MOE_ERR_INVALID_ARG;
+  if (d->k > d->E || d->k > 32) return MOE_ERR_INVALID_ARG;
+  if (d->E > 1024) return MOE_ERR_UNSUPPORTED;
+  if (d->d % 128 != 0 || d->inter % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(d->T) * d->k > (int64_t(1) << 30)) return MOE_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(d->n_shared) * d->T > (int64_t(1) << 30)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status check_ws(const moe_dims* d, const void* ws, size_t ws_bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < make_layout(*d).total) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+moe_status cuda_ok(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+moe_status launched() { return cuda_ok(cudaGetLastError()); }
+
+#define MOE_TRY(expr)                       \
+  do {                                      \
+    const moe_status _s = (expr);           \
+    if (_s != MOE_OK) return _s;            \
+  } while (0)
+
+// Optional stage timing: records caller-created CUDA events between stages.
+struct Recorder {
+  void* const* ev = nullptr;
+  int n = 0, i = 0;
+  cudaStream_t st = nullptr;
+  moe_status mark() {
+    if (!ev) return MOE_OK;
+    if (i >= n) return MOE_ERR_INVALID_ARG;
+    return cuda_ok(cudaEventRecord(static_cast<cudaEvent_t>(ev[i++]), st));
+  }
+};
+
+// ------------------------------------------------------------------ TMA maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// 2-D K-major operand [rows, K]: boxes of 128 bytes of K by box_rows rows,
+// 128-byte swizzle, zero fill outside the tensor.
+moe_status make_tmap(CUtensorMap* map, const void* base, bool fp8, int64_t rows, int64_t K, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return MOE_ERR_CUDA;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K * (fp8 ? 1 : 2))};
+  const cuuint32_t box[2] = {fp8 ? 128u : 64u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+template <bool FP8, int BN, Epi EPI>
+moe_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int64_t grid,
+                       cudaStream_t st) {
+  if (grid <= 0) return MOE_OK;
+  if (grid > INT_MAX) return MOE_ERR_UNSUPPORTED;
+  constexpr size_t smem = gemm_smem_bytes<FP8, BN>();
+  auto kern = grouped_gemm_kernel<FP8, BN, EPI>;
+  MOE_TRY(cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))));
+  kern<<<static_cast<unsigned>(grid), GemmShape<FP8>::THREADS, smem, st>>>(ta, tb, a);
+  return launched();
+}
+
+GemmArgs base_args(int* status) {
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.status = status;
+  return a;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Upper bound of the 128-row tiles of `groups` groups holding `rows` rows.
+int64_t mt_bound(int64_t rows, int64_t groups) { return cdiv(rows + 127 * groups, 128); }
+
+// ------------------------------------------------------------------ pieces
+// Router logits (tcgen05 GEMM, bf16 in, fp32 out) then the warp-per-token top-k.
+moe_status enqueue_route(const moe_dims& d, const uint16_t* u, const uint16_t* cent, const float* bias, int32_t* idx,
+                         float* gate, int32_t* counts, uint32_t* mask, float* z, int* status, cudaStream_t st,
+                         Recorder* rec = nullptr) {
+  const int W = (d.T + 31) / 32;
+  MOE_TRY(cuda_ok(cudaMemsetAsync(counts, 0, sizeof(int32_t) * d.E, st)));
+  CUtensorMap ta, tb;
+  MOE_TRY(make_tmap(&ta, u, false, d.T, d.d, 128));
+  MOE_TRY(make_tmap(&tb, cent, false, d.E, d.d, 128));
+  GemmArgs a = base_args(status);
+  a.n_groups = 1;
+  a.uni_m = d.T;
+  a.N = d.E;
+  a.K = d.d;
+  a.b_rows_per_group = d.E;
+  a.a_rows_cap = d.T;
+  a.out = z;
+  a.out_ld = d.E;
+  MOE_TRY((launch_gemm<false, 128, Epi::F32>(ta, tb, a, cdiv(d.T, 128) * cdiv(d.E, 128), st)));
+  if (rec) MOE_TRY(rec->mark());
+  const unsigned blocks = static_cast<unsigned>(cdiv(int64_t(d.T) * 32, 256));
+  const int vpl = (d.E + 31) / 32;
+#define MOE_TOPK(V) route_topk_kernel<V><<<blocks, 256, 0, st>>>(z, d.T, d.E, d.k, bias, idx, gate, counts, mask, W)
+  if (vpl <= 1) MOE_TOPK(1);
+  else if (vpl <= 2) MOE_TOPK(2);
+  else if (vpl <= 4) MOE_TOPK(4);
+  else if (vpl <= 8) MOE_TOPK(8);
+  else if (vpl <= 16) MOE_TOPK(16);
+  else MOE_TOPK(32);
+#undef MOE_TOPK
+  MOE_TRY(launched());
+  return rec ? rec->mark() : MOE_OK;
+}
+
+// Expert row counts and offsets from the token-expert mask, the GEMM group
+// table, and the gather of permuted rows (FP8: quantised on the way).
+moe_status enqueue_dispatch(const moe_dims& d, const int32_t* idx, const uint16_t* u, const uint32_t* mask,
+                            int32_t* wprefix, int32_t* cnt, int32_t* offsets, GroupEntry* groups, int32_t* mt_total,
+                            int32_t* perm, int32_t* slot, void* x, float* xs, uint8_t* uq, float* uqs, int* status,
+                            cudaStream_t st, Recorder* rec = nullptr) {
+  const int W = (d.T + 31) / 32;
+  expert_scan_kernel<<<d.E, 256, 0, st>>>(mask, W, wprefix, cnt);
+  MOE_TRY(launched());
+  plan_kernel<<<1, 1024, 0, st>>>(cnt, nullptr, d.E, 0, offsets, groups, mt_total, status);
+  MOE_TRY(launched());
+  if (rec) MOE_TRY(rec->mark());
+  const unsigned blocks = static_cast<unsigned>(cdiv(int64_t(d.T) * 32, 256));
+  const int64_t rows = int64_t(d.T) * d.k;
+  const __nv_bfloat16* ub = reinterpret_cast<const __nv_bfloat16*>(u);
+  if (d.prec == MOE_FP8_E4M3)
+    dispatch_kernel<true><<<blocks, 256, 0, st>>>(idx, d.T, d.k, d.E, mask, wprefix, W, offsets, slot, perm, ub, d.d,
+                                                  x, xs, rows, uq, uqs);
+  else
+    dispatch_kernel<false><<<blocks, 256, 0, st>>>(idx, d.T, d.k, d.E, mask, wprefix, W, offsets, slot, perm, ub,
+                                                   d.d, x, nullptr, rows, nullptr, nullptr);
+  MOE_TRY(launched());
+  return rec ? rec->mark() : MOE_OK;
+}
+
+// Gate/up (+SwiGLU) then down GEMMs over a set of groups.
+//   table != nullptr: routed experts, rows from the device table (upper bound
+//   rows_cap rows over n_groups groups).  Otherwise n_groups uniform groups of
+//   uni_m rows each; gate/up A rows start at 0 for every group (all shared
+//   experts read the same tokens).
+struct FfnOperands {
+  const void* x;
+  const float* xs;
+  int64_t x_rows;  // rows allocated in x
+  const void* w13;
+  const float* w13s;
+  const void* w2;
+  const float* w2s;
+  void* h;
+  float* hs;
+  uint16_t* y;
+  int64_t rows_cap;  // rows allocated in h and y
+};
+
+moe_status enqueue_ffn(const moe_dims& d, const FfnOperands& o, int n_groups, const GroupEntry* table,
+                       const int32_t* mt_total, int uni_m, int* status, cudaStream_t st, Recorder* rec = nullptr) {
+  const bool fp8 = d.prec == MOE_FP8_E4M3;
+  const int I = d.inter, D = d.d;
+  CUtensorMap ta1, tb1, ta2, tb2;
+  MOE_TRY(make_tmap(&ta1, o.x, fp8, o.x_rows, D, 128));
+  MOE_TRY(make_tmap(&tb1, o.w13, fp8, int64_t(n_groups) * 2 * I, D, 256));
+  MOE_TRY(make_tmap(&ta2, o.h, fp8, o.rows_cap, I, 128));
+  MOE_TRY(make_tmap(&tb2, o.w2, fp8, int64_t(n_groups) * D, I, 256));
+  const int64_t mt = table ? mt_bound(o.rows_cap, n_groups) : int64_t(n_groups) * cdiv(uni_m, 128);
+
+  GemmArgs a = base_args(status);
+  a.groups = table;
+  a.mt_total = mt_total;
+  a.n_groups = n_groups;
+  a.uni_m = uni_m;
+  a.uni_a_step = 0;
+  a.uni_out_step = uni_m;
+  a.N = 2 * I;
+  a.K = D;
+  a.b_rows_per_group = 2 * I;
+  a.a_rows_cap = static_cast<int32_t>(o.x_rows);
+  a.out = o.h;
+  a.out_ld = I;
+  a.a_scale = o.xs;
+  a.a_scale_ld = o.x_rows;
+  a.b_scale = o.w13s;
+  a.out_scale = o.hs;
+  a.out_scale_ld = o.rows_cap;
+  const int64_t g1 = mt * (2 * I / 256);
+  if (fp8) MOE_TRY((launch_gemm<true, 256, Epi::SWIGLU>(ta1, tb1, a, g1, st)));
+  else MOE_TRY((launch_gemm<false, 256, Epi::SWIGLU>(ta1, tb1, a, g1, st)));
+  if (rec) MOE_TRY(rec->mark());
+
+  GemmArgs b = a;
+  b.uni_a_step = uni_m;
+  b.N = D;
+  b.K = I;
+  b.b_rows_per_group = D;
+  b.a_rows_cap = static_cast<int32_t>(o.rows_cap);
+  b.out = o.y;
+  b.out_ld = D;
+  b.a_scale = o.hs;
+  b.a_scale_ld = o.rows_cap;
+  b.b_scale = o.w2s;
+  b.out_scale = nullptr;
+  const int64_t g2 = mt * cdiv(D, 256);
+  if (fp8) MOE_TRY((launch_gemm<true, 256, Epi::BF16>(ta2, tb2, b, g2, st)));
+  else MOE_TRY((launch_gemm<false, 256, Epi::BF16>(ta2, tb2, b, g2, st)));
+  return rec ? rec->mark() : MOE_OK;
+}
+
+moe_status check_weights(const moe_dims& d, const moe_weights* w) {
+  if (!w || !w->w13 || !w->w2 || !w->centroids) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w->w13) || !aligned16(w->w2) || !aligned16(w->centroids)) return MOE_ERR_INVALID_ARG;
+  if (d.n_shared > 0 && (!w->ws13 || !w->ws2 || !aligned16(w->ws13) || !aligned16(w->ws2))) return MOE_ERR_INVALID_ARG;
+  if (d.prec == MOE_FP8_E4M3) {
+    if (!w->w13_scale || !w->w2_scale) return MOE_ERR_INVALID_ARG;
+    if (d.n_shared > 0 && (!w->ws13_scale || !w->ws2_scale)) return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+extern "C" {
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_BAD_INDEX: return "expert index or offset out of range";
+  }
+  return "unknown status";
+}
+
+moe_status moe_workspace_size(const moe_dims* dims, size_t* bytes) {
+  MOE_TRY(check_dims(dims));
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = make_layout(*dims).total;
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_dims* dims, const uint16_t* u, const uint16_t* centroids, const float* bias,
+                     int32_t* topk_idx, float* topk_gate, int32_t* counts, void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_dims(dims));
+  MOE_TRY(check_ws(dims, ws, ws_bytes));
+  if (!u || !centroids || !bias || !topk_idx || !topk_gate || !counts) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(u) || !aligned16(centroids)) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(*dims);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_TRY(cuda_ok(cudaMemsetAsync(at<int>(ws, L.status), 0, sizeof(int), st)));
+  if (dims->T == 0) return cuda_ok(cudaMemsetAsync(counts, 0, sizeof(int32_t) * dims->E, st));
+  return enqueue_route(*dims, u, centroids, bias, topk_idx, topk_gate, counts, nullptr, at<float>(ws, L.z),
+                       at<int>(ws, L.status), st);
+}
+
+moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, const uint16_t* u, int32_t* offsets,
+                       int32_t* perm, int32_t* slot, void* x_perm, float* x_scale, void* ws, size_t ws_bytes,
+                       void* stream) {
+  MOE_TRY(check_dims(dims));
+  MOE_TRY(check_ws(dims, ws, ws_bytes));
+  if (!topk_idx || !u || !offsets || !perm || !slot || !x_perm) return MOE_ERR_INVALID_ARG;
+  if (dims->prec == MOE_FP8_E4M3 && !x_scale) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(u) || !aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(*dims);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* status = at<int>(ws, L.status);
+  MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, sizeof(int), st)));
+  const int W = (dims->T + 31) / 32;
+  uint32_t* mask = at<uint32_t>(ws, L.mask);
+  MOE_TRY(cuda_ok(cudaMemsetAsync(mask, 0, sizeof(uint32_t) * size_t(dims->E) * W, st)));
+  const int64_t n = int64_t(dims->T) * dims->k;
+  if (n > 0) {
+    build_mask_kernel<<<static_cast<unsigned>(cdiv(n, 256)), 256, 0, st>>>(topk_idx, n, dims->k, dims->E, mask, W,
+                                                                           status);
+    MOE_TRY(launched());
+  }
+  return enqueue_dispatch(*dims, topk_idx, u, mask, at<int32_t>(ws, L.wprefix), at<int32_t>(ws, L.cnt), offsets,
+                          at<GroupEntry>(ws, L.groups), at<int32_t>(ws, L.mt_total), perm, slot, x_perm, x_scale,
+                          nullptr, nullptr, status, st);
+}
+
+moe_status moe_grouped_ffn(const moe_dims* dims, int32_t n_groups, int32_t rows, const int32_t* offsets,
+                           const void* x, const float* x_scale, const void* w13, const float* w13_scale,
+                           const void* w2, const float* w2_scale, uint16_t* y, void* ws, size_t ws_bytes,
+                           void* stream) {
+  MOE_TRY(check_dims(dims));
+  MOE_TRY(check_ws(dims, ws, ws_bytes));
+  const bool fp8 = dims->prec == MOE_FP8_E4M3;
+  if (n_groups <= 0 || n_groups > dims->E + dims->n_shared || rows < 0) return MOE_ERR_INVALID_ARG;
+  if (int64_t(rows) > int64_t(dims->T) * dims->k) return MOE_ERR_WORKSPACE;
+  if (!offsets || !x || !w13 || !w2 || !y) return MOE_ERR_INVALID_ARG;
+  if (fp8 && (!x_scale || !w13_scale || !w2_scale)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w13) || !aligned16(w2) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(*dims);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* status = at<int>(ws, L.status);
+  MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, sizeof(int), st)));
+  if (rows == 0) return MOE_OK;
+  GroupEntry* groups = at<GroupEntry>(ws, L.groups);
+  int32_t* mt_total = at<int32_t>(ws, L.mt_total);
+  plan_kernel<<<1, 1024, 0, st>>>(nullptr, offsets, n_groups, rows, nullptr, groups, mt_total, status);
+  MOE_TRY(launched());
+  FfnOperands o{x, x_scale, rows, w13, w13_scale, w2, w2_scale, at<void>(ws, L.h),
+                fp8 ? at<float>(ws, L.hs) : nullptr, y, rows};
+  return enqueue_ffn(*dims, o, n_groups, groups, mt_total, 0, status, st);
+}
+
+moe_status moe_combine(const moe_dims* dims, const uint16_t* u, const uint16_t* shared_y, const uint16_t* y_perm,
+                       const int32_t* slot, const float* topk_gate, uint16_t* out, void* stream) {
+  MOE_TRY(check_dims(dims));
+  if (!u || !y_perm || !slot || !topk_gate || !out || (dims->n_shared > 0 && !shared_y)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(u) || !aligned16(y_perm) || !aligned16(out) || (shared_y && !aligned16(shared_y)))
+    return MOE_ERR_INVALID_ARG;
+  if (dims->T == 0) return MOE_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  combine_kernel<<<dims->T, 128, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(u), reinterpret_cast<const __nv_bfloat16*>(shared_y), dims->n_shared,
+      reinterpret_cast<const __nv_bfloat16*>(y_perm), slot, topk_gate, dims->T, dims->d, dims->k,
+      int64_t(dims->T) * dims->k, reinterpret_cast<__nv_bfloat16*>(out), nullptr);
+  return launched();
+}
+
+moe_status moe_bias_update(int32_t E, int32_t T, int32_t k, const int32_t* counts, float gamma, float* bias,
+                           void* stream) {
+  if (E <= 0 || E > 1024 || T < 0 || k <= 0 || k > E || !counts || !bias) return MOE_ERR_INVALID_ARG;
+  bias_update_kernel<<<static_cast<unsigned>(cdiv(E, 256)), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      E, T, k, counts, gamma, bias);
+  return launched();
+}
+
+moe_status moe_forward(const moe_dims* dims, const moe_weights* w, const uint16_t* u, const float* bias,
+                       uint16_t* out, int32_t* counts_out, void* ws, size_t ws_bytes, void* stream) {
+  return moe_forward_profiled(dims, w, u, bias, out, counts_out, ws, ws_bytes, stream, nullptr, 0);
+}
+
+moe_status moe_forward_profiled(const moe_dims* dims, const moe_weights* w, const uint16_t* u, const float* bias,
+                                uint16_t* out, int32_t* counts_out, void* ws, size_t ws_bytes, void* stream,
+                                void* const* events, int32_t n_events) {
+  MOE_TRY(check_dims(dims));
+  MOE_TRY(check_ws(dims, ws, ws_bytes));
+  MOE_TRY(check_weights(*dims, w));
+  if (!u || !bias || !out || !aligned16(u) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  if (events && n_events < MOE_PROFILE_EVENTS) return MOE_ERR_INVALID_ARG;
+  const moe_dims& d = *dims;
+  const bool fp8 = d.prec == MOE_FP8_E4M3;
+  const Layout L = make_layout(d);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Recorder recorder;
+  recorder.ev = events;
+  recorder.n = n_events;
+  recorder.st = st;
+  Recorder* rec = events ? &recorder : nullptr;
+  if (rec) MOE_TRY(rec->mark());
+  int* status = at<int>(ws, L.status);
+  MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, sizeof(int), st)));
+  int32_t* counts = counts_out ? counts_out : at<int32_t>(ws, L.counts);
+  if (d.T == 0) return cuda_ok(cudaMemsetAsync(counts, 0, sizeof(int32_t) * d.E, st));
+  const int W = (d.T + 31) / 32;
+  uint32_t* mask = at<uint32_t>(ws, L.mask);
+  MOE_TRY(cuda_ok(cudaMemsetAsync(mask, 0, sizeof(uint32_t) * size_t(d.E) * W, st)));
+
+  int32_t* idx = at<int32_t>(ws, L.idx);
+  float* gate = at<float>(ws, L.gate);
+  MOE_TRY(enqueue_route(d, u, w->centroids, bias, idx, gate, counts, mask, at<float>(ws, L.z), status, st, rec));
+
+  GroupEntry* groups = at<GroupEntry>(ws, L.groups);
+  int32_t* mt_total = at<int32_t>(ws, L.mt_total);
+  int32_t* slot = at<int32_t>(ws, L.slot);
+  const int64_t R = int64_t(d.T) * d.k;
+  MOE_TRY(enqueue_dispatch(d, idx, u, mask, at<int32_t>(ws, L.wprefix), at<int32_t>(ws, L.cnt),
+                           at<int32_t>(ws, L.offsets), groups, mt_total, at<int32_t>(ws, L.perm), slot,
+                           at<void>(ws, L.x), fp8 ? at<float>(ws, L.xs) : nullptr,
+                           fp8 ? at<uint8_t>(ws, L.uq) : nullptr, fp8 ? at<float>(ws, L.uqs) : nullptr, status, st,
+                           rec));
+
+  // routed experts: groups from the device table
+  FfnOperands ro{at<void>(ws, L.x), fp8 ? at<float>(ws, L.xs) : nullptr, R, w->w13, w->w13_scale, w->w2,
+                 w->w2_scale, at<void>(ws, L.h), fp8 ? at<float>(ws, L.hs) : nullptr, at<uint16_t>(ws, L.y), R};
+  MOE_TRY(enqueue_ffn(d, ro, d.E, groups, mt_total, 0, status, st, rec));
+
+  // shared experts: every token, n_shared uniform groups
+  uint16_t* ysh = at<uint16_t>(ws, L.ysh);
+  if (d.n_shared > 0) {
+    const void* xa = fp8 ? static_cast<const void*>(at<uint8_t>(ws, L.uq)) : static_cast<const void*>(u);
+    FfnOperands so{xa, fp8 ? at<float>(ws, L.uqs) : nullptr, d.T, w->ws13, w->ws13_scale, w->ws2, w->ws2_scale,
+                   at<void>(ws, L.hsh), fp8 ? at<float>(ws, L.hshs) : nullptr, ysh, int64_t(d.n_shared) * d.T};
+    MOE_TRY(enqueue_ffn(d, so, d.n_shared, nullptr, nullptr, d.T, status, st, rec));
+  } else if (rec) {
+    MOE_TRY(rec->mark());
+    MOE_TRY(rec->mark());
+  }
+
+  combine_kernel<<<d.T, 128, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(u), reinterpret_cast<const __nv_bfloat16*>(ysh), d.n_shared,
+      at<const __nv_bfloat16>(ws, L.y), slot, gate, d.T, d.d, d.k, R, reinterpret_cast<__nv_bfloat16*>(out), status);
+  MOE_TRY(launched());
+  return rec ? rec->mark() : MOE_OK;
+}
+
+moe_status moe_pack_gate_up(const uint16_t* w1, const uint16_t* w3, int32_t E, int32_t inter, int32_t d,
+                            uint16_t* w13, void* stream) {
+  if (!w1 || !w3 || !w13 || E <= 0 || inter <= 0 || d <= 0 || inter % 128 || d % 8) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w1) || !aligned16(w3) || !aligned16(w13)) return MOE_ERR_INVALID_ARG;
+  pack_gate_up_kernel<<<148 * 8, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      reinterpret_cast<const uint4*>(w1), reinterpret_cast<const uint4*>(w3), E, inter, d,
+      reinterpret_cast<uint4*>(w13));
+  return launched();
+}
+
+moe_status moe_quantize_fp8_blocks(const uint16_t* w, int64_t rows, int32_t cols, uint8_t* q, float* scale,
+                                   void* stream) {
+  if (!w || !q || !scale || rows <= 0 || cols <= 0 || rows % 128 || cols % 128) return MOE_ERR_INVALID_ARG;
+  if (rows / 128 > 65535 * 64) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(w) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // grid.y is limited to 65535 block rows: split taller matrices
+  for (int64_t r0 = 0; r0 < rows; r0 += int64_t(65535) * 128) {
+    const int64_t r = rows - r0 < int64_t(65535) * 128 ? rows - r0 : int64_t(65535) * 128;
+    dim3 grid(cols / 128, static_cast<unsigned>(r / 128));
+    quantize_blocks_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(w) + r0 * cols, cols,
+                                                 q + r0 * cols, scale + (r0 / 128) * (cols / 128));
+    MOE_TRY(launched());
+  }
+  return MOE_OK;
+}
+
+moe_status moe_read_device_status(const void* ws, void* stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  return static_cast<moe_status>(v);
+}
+
+moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, int32_t timeout_us, void* stream) {
+  if (!ws || ws_bytes < 256 || timeout_us <= 0 || timeout_us > 10000000) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MOE_TRY(cuda_ok(cudaMemsetAsync(ws, 0, sizeof(int), st)));
+  selftest_timeout_kernel<<<1, 32, 0, st>>>(static_cast<int*>(ws), uint64_t(timeout_us) * 1000ull);
+  return launched();
+}
+
+}  // extern "C"

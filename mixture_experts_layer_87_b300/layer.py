@@ -1,0 +1,86 @@
+"""MoELayer: device-resident weights + workspace of one DeepSeekMoE layer.
+
+Plumbing around the C ABI: torch provides the device memory, the library
+does every step of the layer.  Weights are loaded one expert at a time from
+host tensors (nn.Linear layout: W1, W3 [I, d], W2 [d, I], bf16); the
+gate/up pair is interleaved on the device by moe_pack_gate_up and, for FP8,
+quantised per 128 x 128 block by moe_quantize_fp8_blocks, so a V3-sized
+layer never needs a second full bf16 copy on the device.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import capi
+
+
+class MoELayer:
+    def __init__(self, T: int, d: int, E: int, k: int, n_shared: int, inter: int, prec: str = "bf16",
+                 device: str | torch.device = "cuda"):
+        self.T, self.d, self.E, self.k, self.n_shared, self.inter, self.prec = T, d, E, k, n_shared, inter, prec
+        self.device = torch.device(device)
+        self.fp8 = prec == "fp8"
+        self.dims = capi.dims(T, d, E, k, n_shared, inter, prec)
+        self.ws = torch.empty(capi.moe_workspace_size(self.dims), dtype=torch.uint8, device=self.device)
+        wt = torch.uint8 if self.fp8 else torch.bfloat16
+        dev = self.device
+        self.w13 = torch.empty((E, 2 * inter, d), dtype=wt, device=dev)
+        self.w2 = torch.empty((E, d, inter), dtype=wt, device=dev)
+        self.ws13 = torch.empty((max(n_shared, 1), 2 * inter, d), dtype=wt, device=dev)
+        self.ws2 = torch.empty((max(n_shared, 1), d, inter), dtype=wt, device=dev)
+        if self.fp8:
+            f = torch.float32
+            self.w13_scale = torch.empty((E, 2 * inter // 128, d // 128), dtype=f, device=dev)
+            self.w2_scale = torch.empty((E, d // 128, inter // 128), dtype=f, device=dev)
+            self.ws13_scale = torch.empty((max(n_shared, 1), 2 * inter // 128, d // 128), dtype=f, device=dev)
+            self.ws2_scale = torch.empty((max(n_shared, 1), d // 128, inter // 128), dtype=f, device=dev)
+        else:
+            self.w13_scale = self.w2_scale = self.ws13_scale = self.ws2_scale = None
+        self.centroids = torch.empty((E, d), dtype=torch.bfloat16, device=dev)
+        self._stage13 = torch.empty((2, inter, d), dtype=torch.bfloat16, device=dev)
+        self._stage_pack = torch.empty((2 * inter, d), dtype=torch.bfloat16, device=dev)
+        self._stage2 = torch.empty((d, inter), dtype=torch.bfloat16, device=dev)
+
+    # ------------------------------------------------------------ weights
+    def set_centroids(self, c: torch.Tensor) -> None:
+        self.centroids.copy_(c)
+
+    def load_expert(self, e: int, w1: torch.Tensor, w3: torch.Tensor, w2: torch.Tensor, shared: bool = False):
+        """Upload one expert's bf16 W1, W3 [I, d] and W2 [d, I]."""
+        I, d = self.inter, self.d
+        w13 = (self.ws13 if shared else self.w13)[e]
+        w2d = (self.ws2 if shared else self.w2)[e]
+        self._stage13[0].copy_(w1)
+        self._stage13[1].copy_(w3)
+        if not self.fp8:
+            capi.moe_pack_gate_up(self._stage13[0], self._stage13[1], 1, I, d, w13)
+            w2d.copy_(w2)
+            return
+        capi.moe_pack_gate_up(self._stage13[0], self._stage13[1], 1, I, d, self._stage_pack)
+        s13 = (self.ws13_scale if shared else self.w13_scale)[e]
+        s2 = (self.ws2_scale if shared else self.w2_scale)[e]
+        capi.moe_quantize_fp8_blocks(self._stage_pack, 2 * I, d, w13, s13)
+        self._stage2.copy_(w2)
+        capi.moe_quantize_fp8_blocks(self._stage2, d, I, w2d, s2)
+
+    def release_staging(self) -> None:
+        torch.cuda.current_stream().synchronize()
+        self._stage13 = self._stage_pack = self._stage2 = None
+
+    def weights(self) -> capi.moe_weights:
+        return capi.weights_struct(self.w13, self.w13_scale, self.w2, self.w2_scale,
+                                   self.ws13 if self.n_shared else None,
+                                   self.ws13_scale if self.n_shared else None,
+                                   self.ws2 if self.n_shared else None,
+                                   self.ws2_scale if self.n_shared else None, self.centroids)
+
+    # ------------------------------------------------------------ forward
+    def forward(self, u: torch.Tensor, bias: torch.Tensor, out: torch.Tensor | None = None,
+                counts: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty((self.T, self.d), dtype=torch.bfloat16, device=self.device)
+        capi.moe_forward(self.dims, self.weights(), u, bias, out, counts, self.ws, stream)
+        return out
+
+    def status(self) -> int:
+        return capi.moe_read_device_status(self.ws)

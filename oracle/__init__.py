@@ -242,6 +242,24 @@ def layer_output(u_bits: np.ndarray, tokens: np.ndarray, idx: np.ndarray, gate: 
     return out
 
 
+def combine(u_bits: np.ndarray, shared_y: np.ndarray, y_perm: np.ndarray, slot: np.ndarray,
+            gate: np.ndarray) -> np.ndarray:
+    """out_t = u_t + sum_s shared_y[s, t] + sum_j gate[t, j] y_perm[slot[t, j]], fp64.
+
+    The layer equation of ai.flicky.cc 2.1.2 written over already computed
+    expert outputs: shared_y [N_s, T, d] and y_perm [T*k, d] (any float
+    arrays, widened exactly), slot [T, k], gate [T, k].
+    """
+    out = bf16_to_f64(u_bits)
+    for s in range(shared_y.shape[0]):
+        out = out + np.asarray(shared_y[s], np.float64)
+    T, k = slot.shape
+    yp = np.asarray(y_perm, np.float64)
+    for j in range(k):
+        out = out + np.asarray(gate[:, j], np.float64)[:, None] * yp[slot[:, j]]
+    return out
+
+
 def bias_update(counts: np.ndarray, bias: np.ndarray, T: int, k: int, gamma: float) -> np.ndarray:
     """One auxiliary-loss-free bias step in fp32 (ai.flicky.cc 2.1.2; xyznot.com Method 2)."""
     counts = _c(counts, np.int32)

@@ -1,0 +1,103 @@
+"""The C-ABI library loads without a GPU, exports every symbol include/moe.h
+declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from mixture_experts_layer_87_b300 import build, capi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return capi.lib()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert set(names) == set(capi.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_library_is_sm103a_only(lib):
+    assert "arch=compute_103a,code=sm_103a" in " ".join(build.NVCC_FLAGS)
+
+
+def test_status_strings(lib):
+    assert capi.status_string(0) == "ok"
+    assert "workspace" in capi.status_string(3)
+    assert capi.status_string(99) == "unknown status"
+
+
+def _dims(**kw):
+    base = dict(T=64, d=256, E=16, k=4, n_shared=1, inter=128, prec="bf16")
+    base.update(kw)
+    return capi.dims(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(k=17), 1),           # k > E
+    (dict(E=40, k=33), 1),     # k > 32
+    (dict(E=2000), 2),         # E > 1024
+    (dict(d=200), 2),          # d % 128
+    (dict(inter=100), 2),      # I % 128
+    (dict(T=-1), 1),
+    (dict(prec=7), 1),
+])
+def test_workspace_size_rejects_bad_dims(lib, kw, code):
+    n = ctypes.c_size_t(0)
+    dm = _dims(**kw)
+    assert lib.moe_workspace_size(ctypes.byref(dm), ctypes.byref(n)) == code
+
+
+def test_workspace_size_grows_with_shape(lib):
+    small = capi.moe_workspace_size(_dims())
+    big = capi.moe_workspace_size(_dims(T=8192, d=7168, E=256, k=8, inter=2048))
+    fp8 = capi.moe_workspace_size(_dims(T=8192, d=7168, E=256, k=8, inter=2048, prec="fp8"))
+    assert 0 < small < fp8 < big
+
+
+def test_calls_reject_null_and_small_workspace_without_a_gpu(lib):
+    dm = _dims()
+    need = capi.moe_workspace_size(dm)
+    fake = 1 << 20   # never dereferenced: validation fails first
+    w = capi.moe_weights()
+    # null weights
+    assert lib.moe_forward(ctypes.byref(dm), ctypes.byref(w), fake, fake, fake, None, fake, need, None) == 1
+    # workspace too small
+    assert lib.moe_route(ctypes.byref(dm), fake, fake, fake, fake, fake, fake, fake, need - 256, None) == 3
+    # misaligned workspace
+    assert lib.moe_route(ctypes.byref(dm), fake, fake, fake, fake, fake, fake, fake + 8, need, None) == 1
+    # null u
+    assert lib.moe_route(ctypes.byref(dm), None, fake, fake, fake, fake, fake, fake, need, None) == 1
+    # FP8 permute without scales
+    d8 = _dims(prec="fp8")
+    n8 = capi.moe_workspace_size(d8)
+    assert lib.moe_permute(ctypes.byref(d8), fake, fake, fake, fake, fake, fake, None, fake, n8, None) == 1
+    # grouped ffn: more rows than the workspace was sized for
+    assert lib.moe_grouped_ffn(ctypes.byref(dm), 2, 64 * 4 + 1, fake, fake, None, fake, None, fake, None, fake,
+                               fake, need, None) == 3
+    # bias update: k > E
+    assert lib.moe_bias_update(4, 10, 5, fake, ctypes.c_float(0.001), fake, None) == 1
+    # block quantiser: shape not a multiple of 128
+    assert lib.moe_quantize_fp8_blocks(fake, 100, 128, fake, fake, None) == 1
+    # misaligned bf16 input
+    assert lib.moe_combine(ctypes.byref(dm), fake + 2, fake, fake, fake, fake, fake, None) == 1
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(capi, "_lib", None)
+    monkeypatch.setattr(capi, "LIB_PATH", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        capi.lib()

@@ -1,0 +1,97 @@
+"""Parity at the full V3 sizes, in the launch configuration the bench times:
+routing, counts and permutation of all 8192 tokens bit for bit (near-ties
+excepted), and the layer output on a strided sample of tokens (tokens are
+independent, so per-token parity is exact)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from mixture_experts_layer_87_b300 import capi
+from parity import TOL, HostLayer, bf16_to_np, check_selection, rel_err
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.mark.parametrize("name,n_sample", [("v3", 32), ("v3_fp8", 12)])
+def test_v3_forward_parity_sampled(name, n_sample):
+    cfg = synth.get_config(name)
+    host = HostLayer(cfg, keep_weights=False)
+    layer = host.device_layer()
+    layer.release_staging()
+    u = synth.tokens(cfg)
+    counts = torch.empty(cfg.E, dtype=torch.int32, device=DEV)
+    out = layer.forward(u.to(DEV), host.bias.to(DEV), counts=counts)
+    assert layer.status() == 0
+    # routing and dispatch of the whole batch
+    dm = layer.dims
+    idx = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=DEV)
+    gate = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=DEV)
+    cnt = torch.empty(cfg.E, dtype=torch.int32, device=DEV)
+    capi.moe_route(dm, u.to(DEV), layer.centroids, host.bias.to(DEV), idx, gate, cnt, layer.ws)
+    R = cfg.T * cfg.k
+    offsets = torch.empty(cfg.E + 1, dtype=torch.int32, device=DEV)
+    perm = torch.empty(R, dtype=torch.int32, device=DEV)
+    slot = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=DEV)
+    fp8 = cfg.prec == "fp8"
+    x = torch.empty((R, cfg.d), dtype=torch.uint8 if fp8 else torch.bfloat16, device=DEV)
+    xs = torch.empty((cfg.d // 128, R), dtype=torch.float32, device=DEV) if fp8 else None
+    capi.moe_permute(dm, idx, u.to(DEV), offsets, perm, slot, x, xs, layer.ws)
+    assert capi.moe_read_device_status(layer.ws) == 0
+    idx_np = idx.cpu().numpy()
+    ub = synth.bf16_bits(u)
+    r = oracle.route(ub, synth.bf16_bits(host.cent), np.asarray(host.bias), cfg.k, want_all=True)
+    ties = check_selection(idx_np, r, np.asarray(host.bias), cfg.k)
+    print(f"{name}: {len(ties)} near-tie tokens of {cfg.T}")
+    lay = oracle.dispatch_layout(idx_np, cfg.E)
+    np.testing.assert_array_equal(counts.cpu().numpy(), lay["counts"])
+    np.testing.assert_array_equal(offsets.cpu().numpy(), lay["offsets"])
+    np.testing.assert_array_equal(perm.cpu().numpy(), lay["perm"])
+    np.testing.assert_array_equal(slot.cpu().numpy(), lay["slot"])
+    # the layer output on a strided sample
+    sample = np.arange(0, cfg.T, cfg.T // n_sample)[:n_sample]
+    g = oracle.gates_for(r["s_all"][sample], idx_np[sample])
+    ref = oracle.layer_output(ub, sample, idx_np[sample], g, host.routed_bits, host.shared_bits, cfg.n_shared,
+                              cfg.E, fp8=fp8)
+    got = bf16_to_np(out)[sample]
+    uref = oracle.bf16_to_f64(ub[sample])
+    err, err_ffn = rel_err(got, ref), rel_err(got - uref, ref - uref)
+    print(f"{name}: max|err|/rms h' = {err:.3e}, on h'-u = {err_ffn:.3e}")
+    assert err <= TOL[cfg.prec]
+    assert err_ffn <= 2 * TOL[cfg.prec]
+
+
+def test_decode_loop_bias_trajectory():
+    """50 decode steps with the bias update between them: the fp32 bias
+    trajectory matches the oracle's bit for bit (on near-tie steps the
+    oracle takes the GPU's validated selection), and the load evens out."""
+    cfg = synth.get_config("decode", d=512, E=64, k=6, inter=256)
+    host = HostLayer(cfg)
+    layer = host.device_layer()
+    b_dev = torch.zeros(cfg.E, dtype=torch.float32, device=DEV)
+    b_ref = np.zeros(cfg.E, np.float32)
+    counts = torch.empty(cfg.E, dtype=torch.int32, device=DEV)
+    cent = synth.bf16_bits(host.cent)
+    ratios = []
+    for step in range(cfg.steps):
+        u = synth.tokens(cfg, step=step)
+        layer.forward(u.to(DEV), b_dev, counts=counts)
+        idx = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=DEV)
+        gate = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=DEV)
+        cnt = torch.empty(cfg.E, dtype=torch.int32, device=DEV)
+        capi.moe_route(layer.dims, u.to(DEV), layer.centroids, b_dev, idx, gate, cnt, layer.ws)
+        capi.moe_bias_update(cfg.E, cfg.T, cfg.k, counts, cfg.gamma, b_dev)
+        assert capi.moe_read_device_status(layer.ws) == 0
+        np.testing.assert_array_equal(cnt.cpu().numpy(), counts.cpu().numpy())
+        r = oracle.route(synth.bf16_bits(u), cent, b_ref, cfg.k, want_all=True)
+        idx_np = idx.cpu().numpy()
+        ties = check_selection(idx_np, r, b_ref, cfg.k)
+        sel = idx_np if ties else r["idx"]
+        c_ref = np.bincount(sel.ravel(), minlength=cfg.E).astype(np.int32)
+        np.testing.assert_array_equal(counts.cpu().numpy(), c_ref)
+        b_ref = oracle.bias_update(c_ref, b_ref, cfg.T, cfg.k, cfg.gamma)
+        np.testing.assert_array_equal(b_dev.cpu().numpy(), b_ref)
+        ratios.append(c_ref.max() / (cfg.T * cfg.k / cfg.E))
+    assert np.mean(ratios[-5:]) < np.mean(ratios[:5])

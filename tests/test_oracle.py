@@ -345,3 +345,24 @@ def test_param_count_closed_forms():
     assert abs(active / 1e9 - gold["active_expert_params_billions_printed"]) < gold["active_rounding_billions"]
     # 256 routed experts of one layer in bf16
     assert 256 * per * 2 == 22_548_578_304
+
+
+def test_combine_matches_layer_assembly():
+    """The combine over per-expert outputs equals the expert-major layer sum
+    (itself pinned to the dense brute force above)."""
+    cfg = synth.get_config("ragged")
+    u, c, b, routed, shared = _tiny_layer(cfg)
+    ub = synth.bf16_bits(u)
+    r = oracle.route(ub, synth.bf16_bits(c), np.asarray(b), cfg.k)
+    lay = oracle.dispatch_layout(r["idx"], cfg.E)
+    x = oracle.bf16_to_f64(ub)
+    y_perm = np.zeros((cfg.T * cfg.k, cfg.d))
+    for e in range(cfg.E):
+        rows = np.arange(lay["offsets"][e], lay["offsets"][e + 1])
+        w1, w3, w2 = oracle.expert_operands(*_bits(routed[e]), fp8=False)
+        y_perm[rows] = oracle.swiglu(x[lay["perm"][rows]], w1, w3, w2)
+    ysh = np.stack([oracle.swiglu(x, *oracle.expert_operands(*_bits(w), fp8=False)) for w in shared])
+    got = oracle.combine(ub, ysh, y_perm, lay["slot"], r["gate"])
+    ref = oracle.layer_output(ub, np.arange(cfg.T), r["idx"], r["gate"], lambda e: _bits(routed[e]),
+                              lambda s: _bits(shared[s]), cfg.n_shared, cfg.E)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12 * np.abs(ref).max())
