@@ -411,9 +411,15 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="v3", choices=["v3", "v3_fp8", "mid", "decode"])
     ap.add_argument("--no-variants", action="store_true", help="skip the FP8 and decode measurements")
+    ap.add_argument("--prec", default=None, choices=["bf16", "fp8"], help="override the workload's precision")
     ap.add_argument("--cpu-tokens", type=int, default=32, help="tokens in the CPU-oracle baseline sample")
     ap.add_argument("--ref-tokens", type=int, default=4, help="tokens per step of the reference arm")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="only build the layer and run warmup+steps forwards (the command ncu wraps)")
     args = ap.parse_args()
+    if args.profile_case:
+        profile_case(args)
+        return
     args.warmup = max(args.warmup, 3)
 
     if args.impl == "reference":
@@ -494,6 +500,27 @@ def main():
             "variants": variants,
         }
         print(json.dumps(line), flush=True)
+
+
+def profile_case(args):
+    """The program ncu wraps: build the workload's layer, run warmup + steps
+    forwards (launch order per forward: router GEMM, top-k, scan, plan,
+    gather, routed gate/up GEMM, routed down GEMM, shared gate/up GEMM, shared
+    down GEMM, combine), check the device status, exit."""
+    torch.cuda.set_device(0)
+    cfg = synth.get_config(args.workload, **({"prec": args.prec} if args.prec else {}))
+    layer = build_layer(cfg)
+    u = synth.tokens(cfg).cuda()
+    bias = synth.bias(cfg).cuda()
+    out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+    for _ in range(args.warmup + args.steps):
+        layer.forward(u, bias, out)
+    torch.cuda.synchronize()
+    st = layer.status()
+    print(json.dumps({"profile_case": cfg.name, "prec": cfg.prec, "forwards": args.warmup + args.steps,
+                      "status": st}))
+    if st != 0:
+        sys.exit(1)
 
 
 def _retarget(layer, cfg):
