@@ -21,7 +21,8 @@
  * Conventions shared by every call
  *   Memory     Every pointer is DEVICE memory owned by the caller, unless a
  *              parameter says otherwise.  The library allocates nothing and
- *              keeps no mutable global state; each call only enqueues work.
+ *              keeps no mutable global state (the one exception is the fixed
+ *              scratch array of moe_route_noalloc); each call only enqueues work.
  *              Base pointers must be 16-byte aligned.
  *   Streams    `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *              default stream).  Calls are asynchronous on that stream.
@@ -116,6 +117,43 @@ moe_status moe_workspace_size(const moe_dims* dims, size_t* bytes);
 moe_status moe_route(const moe_dims* dims, const uint16_t* u, const uint16_t* centroids,
                      const float* bias, int32_t* topk_idx, float* topk_gate, int32_t* counts,
                      void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_route for callers that cannot allocate device memory.  (A library
+ * addition with no counterpart in the paper.)
+ *
+ * Who needs it: code that may not call cudaMalloc -- for example a plugin
+ * running inside a host engine that owns all device memory through its own
+ * pool, or a serving process that reserves every byte at start-up and must
+ * not allocate on the request path, where cudaMalloc can stall the device and
+ * can fail under memory pressure.  Such a caller has no way to obtain the
+ * workspace moe_route wants.
+ *
+ * This variant does the same work with the same kernels and results, but its
+ * scratch (the [T, E] fp32 router logits) lives in a fixed array inside the
+ * library (a `static __device__` array of MOE_ROUTE_NOALLOC_MAX_LOGITS floats,
+ * 8 MiB, 256-byte aligned).  The CUDA runtime places that array on every
+ * device that loads the library and keeps it until the process exits.  The
+ * call itself allocates nothing and calls no allocating routine.
+ *
+ *   u, centroids, bias, topk_idx, topk_gate, counts  as in moe_route.
+ *   device_status  optional [1] int32 device word (NULL: not reported): set to
+ *                  MOE_OK by the call, MOE_ERR_TIMEOUT if a bounded wait in
+ *                  the logits GEMM ran out.
+ * Limits: T * E <= MOE_ROUTE_NOALLOC_MAX_LOGITS, else MOE_ERR_UNSUPPORTED is
+ * returned and nothing is enqueued; other limits as moe_route.
+ * Set-up: the first call on a device (the current device) looks up the
+ * device address of the array with cudaGetSymbolAddress and caches it; make
+ * that first call on each device before any stream capture begins.
+ * Sharing: every call on a device uses the same array, whose content is
+ * whatever the last call left (every logit read is first written by the same
+ * call).  Calls whose work overlaps on the GPU -- on different streams, or
+ * from different host threads -- race on the array: serialise them.
+ */
+#define MOE_ROUTE_NOALLOC_MAX_LOGITS (1 << 21)
+moe_status moe_route_noalloc(const moe_dims* dims, const uint16_t* u, const uint16_t* centroids,
+                             const float* bias, int32_t* topk_idx, float* topk_gate, int32_t* counts,
+                             int32_t* device_status, void* stream);
 
 /*
  * Dropless dispatch (ai.flicky.cc 2.1.2: no token is dropped): groups the

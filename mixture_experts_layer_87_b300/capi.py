@@ -20,7 +20,7 @@ MOE_BF16, MOE_FP8_E4M3 = 0, 1
 
 # Every symbol include/moe.h declares.
 EXPORTS = (
-    "moe_status_string", "moe_workspace_size", "moe_route", "moe_permute", "moe_grouped_ffn",
+    "moe_status_string", "moe_workspace_size", "moe_route", "moe_route_noalloc", "moe_permute", "moe_grouped_ffn",
     "moe_combine", "moe_bias_update", "moe_forward", "moe_forward_profiled", "moe_pack_gate_up",
     "moe_quantize_fp8_blocks",
     "moe_read_device_status", "moe_selftest_wait_timeout",
@@ -61,6 +61,7 @@ def lib() -> ctypes.CDLL:
             "moe_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "moe_workspace_size": ([D, ctypes.POINTER(sz)], ctypes.c_int),
             "moe_route": ([D, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+            "moe_route_noalloc": ([D, vp, vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
             "moe_permute": ([D, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
             "moe_grouped_ffn": ([D, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
             "moe_combine": ([D, vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
@@ -122,6 +123,19 @@ def moe_workspace_size(dm: moe_dims) -> int:
 def moe_route(dm, u, centroids, bias, topk_idx, topk_gate, counts, ws, stream=None):
     _check(lib().moe_route(ctypes.byref(dm), _ptr(u), _ptr(centroids), _ptr(bias), _ptr(topk_idx), _ptr(topk_gate),
                            _ptr(counts), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "moe_route")
+
+
+MOE_ROUTE_NOALLOC_MAX_LOGITS = 1 << 21
+
+
+def moe_route_noalloc(dm, u, centroids, bias, topk_idx, topk_gate, counts, device_status=None, stream=None):
+    """moe_route without a workspace, for callers that cannot allocate device
+    memory: its logits scratch is a fixed array inside the library (T*E at most
+    MOE_ROUTE_NOALLOC_MAX_LOGITS).  device_status: optional int32 device tensor
+    of one element that receives the call's device-side status."""
+    _check(lib().moe_route_noalloc(ctypes.byref(dm), _ptr(u), _ptr(centroids), _ptr(bias), _ptr(topk_idx),
+                                   _ptr(topk_gate), _ptr(counts), _ptr(device_status), _stream(stream)),
+           "moe_route_noalloc")
 
 
 def moe_permute(dm, topk_idx, u, offsets, perm, slot, x_perm, x_scale, ws, stream=None):

@@ -11,6 +11,7 @@
 #include <climits>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "kernels.cuh"
 #include "moe.h"
@@ -534,3 +535,50 @@ moe_status moe_selftest_wait_timeout(void* ws, size_t ws_bytes, int32_t timeout_
 }
 
 }  // extern "C"
+
+// =================================================================== route without a workspace
+// moe_route_noalloc: the router for callers that cannot allocate device memory.
+// Its only scratch, the [T, E] fp32 logits, is this fixed array; the runtime
+// creates it on every device that loads the library.  Host code must not pass
+// the symbol itself to a kernel (on the host it names a stand-in, not device
+// memory): the address comes from cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) float route_logits_scratch[MOE_ROUTE_NOALLOC_MAX_LOGITS];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex scratch_mutex;
+float* scratch_addr[kMaxDevices] = {};
+
+// Device address of route_logits_scratch on the current device, looked up on
+// first use and cached.
+moe_status route_scratch(float** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(scratch_mutex);
+  if (!scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, route_logits_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+    scratch_addr[dev] = static_cast<float*>(p);
+  }
+  *out = scratch_addr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status moe_route_noalloc(const moe_dims* dims, const uint16_t* u, const uint16_t* centroids,
+                                        const float* bias, int32_t* topk_idx, float* topk_gate, int32_t* counts,
+                                        int32_t* device_status, void* stream) {
+  MOE_TRY(check_dims(dims));
+  if (!u || !centroids || !bias || !topk_idx || !topk_gate || !counts) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(u) || !aligned16(centroids)) return MOE_ERR_INVALID_ARG;
+  if (int64_t(dims->T) * dims->E > MOE_ROUTE_NOALLOC_MAX_LOGITS) return MOE_ERR_UNSUPPORTED;
+  float* z = nullptr;
+  MOE_TRY(route_scratch(&z));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (device_status) MOE_TRY(cuda_ok(cudaMemsetAsync(device_status, 0, sizeof(int32_t), st)));
+  if (dims->T == 0) return cuda_ok(cudaMemsetAsync(counts, 0, sizeof(int32_t) * dims->E, st));
+  return enqueue_route(*dims, u, centroids, bias, topk_idx, topk_gate, counts, nullptr, z, device_status, st);
+}
