@@ -38,7 +38,7 @@ METRIC = "MoE layer tokens/s at V3 shape (bf16, FP8); % of tensor/HBM roofline"
 UNIT = "tokens/s"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "mixture_experts_layer_87_b300", "csrc", f)
-                  for f in ("gemm.cuh", "ptx.cuh", "kernels.cuh", "moe_api.cu")]
+                  for f in ("gemm.cuh", "expert_gemm.cuh", "fp8_gemm.cuh", "ptx.cuh", "kernels.cuh", "moe_api.cu")]
 
 
 # ----------------------------------------------------------------------------
@@ -391,6 +391,7 @@ def measure_decode(args, world, pk, layer=None):
     barrier(world)
     step_ms = [ev[s].elapsed_time(ev[s + 1]) for s in range(cfg.steps)]
     total = max_over_ranks(sum(step_ms), world)
+    stage_ms = time_stages(layer, us[0], bias, out, 5)
     c = counts.cpu().numpy()
     mean = cfg.T * cfg.k / cfg.E
     gbs = [layer_work(cfg, c[s])[1] / (step_ms[s] * 1e-3) / 1e9 for s in range(cfg.steps)]
@@ -399,6 +400,7 @@ def measure_decode(args, world, pk, layer=None):
             "hbm_frac_of_measured": round(float(np.mean(gbs)) / pk["hbm"], 4),
             "max_over_mean_load_first": round(float(c[0].max() / mean), 3),
             "max_over_mean_load_last": round(float(c[-1].max() / mean), 3),
+            "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
             "per_step": [{"ms": round(m, 4), "hbm_gbs": round(g, 1), "max_over_mean": round(float(x.max() / mean), 3)}
                          for m, g, x in zip(step_ms, gbs, c)]}
 
@@ -409,7 +411,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="v3", choices=["v3", "v3_fp8", "mid", "decode"])
+    ap.add_argument("--workload", default="v3", choices=["v3", "v3_fp8", "mid", "decode", "v3_slice", "v3_slice_fp8"])
     ap.add_argument("--no-variants", action="store_true", help="skip the FP8 and decode measurements")
     ap.add_argument("--prec", default=None, choices=["bf16", "fp8"], help="override the workload's precision")
     ap.add_argument("--cpu-tokens", type=int, default=32, help="tokens in the CPU-oracle baseline sample")

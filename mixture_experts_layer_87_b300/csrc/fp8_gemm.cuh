@@ -1,0 +1,348 @@
+// Persistent grouped FP8 expert GEMM on the tcgen05 tensor cores (sm_103a):
+// the fine-grained FP8 scheme of ai.flicky.cc section 3.3 (items 2-3).
+//
+//   out[rows of group g] = epilogue( sum_kb  P_kb * s_x[row, kb] * s_w[block, kb] )
+//   P_kb = X_q[rows, 128 kb .. 128 kb + 128) . W_q,g[cols, same K]^T   (E4M3 codes)
+//
+// Tokens sit on the 128 TMEM lanes (one row per lane) and weight rows on the
+// columns, so the activation tile scale s_x of a lane is one number per
+// 128-wide K block and the weight block scale s_w one number per 128 columns:
+// the promotion of a 128-K partial into fp32 costs one FMA per element.
+//
+// Work item = (group g, 256-column weight block n, 128-row tile m), m
+// fastest; one CTA per SM takes items from a shared queue (warp 10 fetches
+// and decodes them, see the item ring of expert_gemm.cuh).  Warp 0
+// issues TMA loads into a 4-stage ring (16 KB of tokens + 32 KB of weights
+// per 128-K stage), one thread of warp 1 issues kind::f8f6f4 MMAs (K = 32)
+// into one of two TMEM partial buffers (2 x 256 columns), warps 2..9 promote:
+// the warp of lane quarter q and column half c reads 16-column slices of the
+// partial (the next slice's tcgen05.ld in flight during the current FMAs),
+// multiplies by s_x * s_w and adds into 128 fp32 registers, then frees the
+// buffer for the MMA two K blocks ahead.  Warps whose 32 rows all lie past
+// the group's end keep the barrier phases in step without loading anything.
+//
+// Epilogues:
+//   SWIGLU  the weight block holds 128 gate rows then the 128 matching up
+//           rows (w13 interleave): h = SiLU(gate) * up for 128 features,
+//           quantised per row over those 128 features (scale = amax/448,
+//           E4M3 codes, the 1 x 128 activation tile of the down GEMM).
+//   BF16    y as bf16.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "expert_gemm.cuh"
+#include "gemm.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+struct F8Shape {
+  static constexpr int BM = 128, BN = 256, BK = 128, UK = 32;
+  static constexpr uint32_t A_BYTES = BM * 128, B_BYTES = BN * 128;
+  static constexpr int STAGES = 4;
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int THREADS = 32 * (3 + EPI_WARPS);  // producer, MMA, epilogue, scheduler
+};
+
+constexpr size_t fp8_gemm_smem_bytes() {
+  return 1024 + size_t(F8Shape::STAGES) * (F8Shape::A_BYTES + F8Shape::B_BYTES) + 512 /* barriers, item ring */ +
+         2 * 2 * 128 * sizeof(float) /* amax exchange: 2 items x 2 halves x 128 rows */;
+}
+
+// Item -> (group, column block, row tile); the same ordering and table as
+// the bf16 expert GEMM (chunks of 128 rows).
+__device__ __forceinline__ bool f8decode(const GemmArgs& a, int tile, int items, int nb, TileCoord& tc) {
+  constexpr int BM = 128;
+  if (tile >= items) return false;
+  if (a.groups == nullptr) {
+    const int mt = (a.uni_m + BM - 1) / BM;
+    const int per_group = mt * nb;
+    tc.g = tile / per_group;
+    const int local = tile - tc.g * per_group;
+    tc.n_idx = local / mt;
+    tc.m_idx = local - tc.n_idx * mt;
+    tc.a_row = tc.g * a.uni_a_step + tc.m_idx * BM;
+    tc.out_row = tc.g * a.uni_out_step + tc.m_idx * BM;
+    tc.rows_valid = min(BM, a.uni_m - tc.m_idx * BM);
+    return true;
+  }
+  const int g = __ldg(a.chunk_group + tile / nb);
+  const int4 G = __ldg(reinterpret_cast<const int4*>(a.groups) + g);  // {a_row0, out_row0, m, mt_start}
+  const int mt = (G.z + BM - 1) / BM;
+  const int local = tile - G.w * nb;
+  tc.g = g;
+  tc.n_idx = local / mt;
+  tc.m_idx = local - tc.n_idx * mt;
+  tc.a_row = G.x + tc.m_idx * BM;
+  tc.out_row = G.y + tc.m_idx * BM;
+  tc.rows_valid = min(BM, G.z - tc.m_idx * BM);
+  return true;
+}
+
+template <Epi EPI>
+__global__ void __launch_bounds__(F8Shape::THREADS, 1)
+    fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const GemmArgs args) {
+  using S = F8Shape;
+  constexpr int BN = S::BN, STAGES = S::STAGES;
+  constexpr uint32_t A_BYTES = S::A_BYTES, B_BYTES = S::B_BYTES;
+  constexpr uint32_t TMEM_COLS = 2 * BN;
+  static_assert(EPI == Epi::SWIGLU || EPI == Epi::BF16, "FP8 epilogues");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;  // [2] partial buffer written
+  uint64_t* acc_empty = acc_full + 2;   // [2] partial buffer drained (8 warps)
+  uint64_t* pair_bar = acc_empty + 2;   // [4] the two warps of one lane quarter
+  uint64_t* mma_done = pair_bar + 4;
+  ItemRing ring;
+  ring.q_full = mma_done + 1;
+  ring.q_empty = ring.q_full + kQueueSlots;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ring.q_empty + kQueueSlots);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  ring.slot = reinterpret_cast<int*>(tmem_slot + 4);
+  float* amax_x = reinterpret_cast<float*>(smem + STAGES * (A_BYTES + B_BYTES) + 512);  // [2][2][128]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nb = (args.N + BN - 1) / BN;
+  const int num_kb = args.K / S::BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], S::EPI_WARPS);
+    }
+    for (int q = 0; q < 4; ++q) mbar_init(&pair_bar[q], 2);
+    for (int q = 0; q < kQueueSlots; ++q) {
+      mbar_init(&ring.q_full[q], 1);
+      mbar_init(&ring.q_empty[q], 2 + S::EPI_WARPS);  // producer, MMA thread, epilogue warps
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 10) {
+    // ------------------------------------------------------------ item scheduler
+    if (lane == 0) {
+      const int items = args.groups == nullptr ? (args.uni_m + 127) / 128 * nb * args.n_groups
+                                               : __ldg(args.mt_total) * nb;
+      int item = blockIdx.x;
+      for (uint32_t lt = 0;; ++lt) {
+        TileCoord tc{-1, 0, 0, 0, 0, 0};
+        const bool have = f8decode(args, item, items, nb, tc);
+        if (have) item = gridDim.x + atomicAdd(args.queue, 1);  // the next one, while this one is published
+        const int v[6] = {have ? tc.g : -1, tc.m_idx, tc.n_idx, tc.a_row, tc.out_row, tc.rows_valid};
+        if (!ring_put(ring, lt, v, args.status, abort_flag) || !have) break;
+      }
+    }
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t it = 0, issued = 0;
+      for (uint32_t lt = 0;; ++lt) {
+        int v[6];
+        if (!ring_take(ring, lt, v, args.status, abort_flag, false) || v[0] < 0) break;
+        const int b_row = v[0] * args.b_rows_per_group + v[2] * BN, a_row = v[3];
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb, ++it) {
+          const uint32_t s = it % STAGES;
+          if (it >= STAGES && !xwait(&empty[s], ((it / STAGES) & 1) ^ 1, args.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
+          tma_load_2d(sA + s * A_BYTES, &tmA, kb * S::BK, a_row, &full[s]);
+          tma_load_2d(sB + s * B_BYTES, &tmB, kb * S::BK, b_row, &full[s]);
+          issued = it + 1;
+        }
+        if (!ok) break;
+      }
+      // Abnormal exit only: copies still in flight land before the CTA leaves.
+      if (*abort_flag)
+        for (uint32_t j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
+          mbar_wait(&full[j % STAGES], (j / STAGES) & 1, args.status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_make(0u, 128, BN);  // E4M3 x E4M3 -> fp32, M = 128, N = 256
+      uint32_t it = 0;
+      bool ok = true;
+      // the MMAs need no item coordinates (the producer placed the operands),
+      // only where the item stream ends
+      for (uint32_t lt = 0; ok; ++lt) {
+        int v[6];
+        if (!ring_take(ring, lt, v, args.status, abort_flag, false)) {
+          ok = false;
+          break;
+        }
+        if (v[0] < 0) break;
+        for (int kb = 0; kb < num_kb && ok; ++kb, ++it) {
+          const uint32_t s = it % STAGES, b = it & 1, u = it >> 1;
+          ok = xwait(&full[s], (it / STAGES) & 1, args.status, abort_flag);
+          if (ok && u > 0) ok = xwait(&acc_empty[b], (u & 1) ^ 1, args.status, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + s * A_BYTES), b0 = smem_u32(sB + s * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < S::BK / S::UK; ++k)
+            mma_fp8(tmem_base + b * BN, sdesc_k128(a0 + k * 32), sdesc_k128(b0 + k * 32), idesc, k > 0 ? 1u : 0u);
+          mma_commit(&empty[s]);
+          mma_commit(&acc_full[b]);
+        }
+      }
+      if (!ok) *abort_flag = 1;
+      mma_commit(mma_done);  // every MMA of this CTA has completed before TMEM is released
+      mbar_wait(mma_done, 0, args.status);
+    }
+  } else {
+    // ------------------------------------------------------------ promotion + epilogue
+    const int ew = warp - 2;
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int half = ew >> 2;      // SWIGLU: gate [64h, 64h+64) + up 128 + [64h, ..); plain: cols [128h, 128h+128)
+    const int r = quarter * 32 + lane;
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int KB = args.K / 128;
+    uint32_t it = 0, pphase = 0;
+    bool ok = true;
+    for (uint32_t lt = 0;; ++lt) {
+      int v[6];
+      if (!ring_take(ring, lt, v, args.status, abort_flag, true)) {
+        ok = false;
+        break;
+      }
+      if (v[0] < 0) break;
+      const TileCoord tc{v[0], v[1], v[2], v[3], v[4], v[5]};
+      const bool row_ok = r < tc.rows_valid;
+      const bool warp_rows = quarter * 32 < tc.rows_valid;
+      const int a_row = tc.a_row + r;
+      const bool a_in = a_row < args.a_rows_cap;
+      const float* sa_ptr = args.a_scale + a_row;
+      const int b_row = tc.g * args.b_rows_per_group + tc.n_idx * BN;
+      const float* sb_ptr = args.b_scale + (int64_t)(b_row / 128) * KB;
+      const bool half_ok = EPI == Epi::SWIGLU || tc.n_idx * BN + half * 128 < args.N;
+      const float* sb0_ptr = sb_ptr + (EPI == Epi::SWIGLU ? 0 : (int64_t)half * KB);
+      const float* sb1_ptr = sb_ptr + (EPI == Epi::SWIGLU ? KB : (int64_t)half * KB);
+      float sa_next = a_in ? __ldg(sa_ptr) : 0.0f;
+      float sb0_next = half_ok ? __ldg(sb0_ptr) : 0.0f, sb1_next = half_ok ? __ldg(sb1_ptr) : 0.0f;
+      float acc[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+#pragma unroll 1
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        const uint32_t b = it & 1, u = it >> 1;
+        const float s0 = sa_next * sb0_next, s1 = sa_next * sb1_next;
+        if (kb + 1 < num_kb) {  // scales one K block ahead
+          sa_next = a_in ? __ldg(sa_ptr + (int64_t)(kb + 1) * args.a_scale_ld) : 0.0f;
+          sb0_next = half_ok ? __ldg(sb0_ptr + kb + 1) : 0.0f;
+          sb1_next = half_ok ? __ldg(sb1_ptr + kb + 1) : 0.0f;
+        }
+        ok = __all_sync(0xffffffffu, xwait(&acc_full[b], u & 1, args.status, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t tb = t_lane + b * BN;
+        if (warp_rows) {
+          auto col_of = [&](int j) -> uint32_t {
+            if constexpr (EPI == Epi::SWIGLU)
+              return j < 4 ? half * 64 + j * 16 : 128 + half * 64 + (j - 4) * 16;
+            else
+              return half * 128 + j * 16;
+          };
+          uint32_t va[16], vb[16];
+          tmem_ld16_nowait(tb + col_of(0), va);
+          tmem_ld_wait(va);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint32_t(&cur)[16] = (j & 1) ? vb : va;
+            uint32_t(&nxt)[16] = (j & 1) ? va : vb;
+            if (j + 1 < 8) tmem_ld16_nowait(tb + col_of(j + 1), nxt);
+            const float sc = (EPI == Epi::SWIGLU && j >= 4) ? s1 : s0;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[j * 16 + i] = fmaf(__uint_as_float(cur[i]), sc, acc[j * 16 + i]);
+            if (j + 1 < 8) tmem_ld_wait(nxt);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[b]);
+      }
+      if (!ok) break;
+      if constexpr (EPI == Epi::SWIGLU) {
+        // h = SiLU(gate) * up for my 64 features; the row's 1 x 128 scale needs
+        // the partner warp's (other column half) amax as well.
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          acc[i] = silu(acc[i]) * acc[64 + i];
+          amax = fmaxf(amax, fabsf(acc[i]));
+        }
+        float* ax = amax_x + (lt & 1) * 256;  // alternate slots: the partner may still read the last item's
+        ax[half * 128 + r] = amax;
+        ok = group_sync(&pair_bar[quarter], pphase, args.status, abort_flag);
+        if (!ok) break;
+        amax = fmaxf(amax, ax[(half ^ 1) * 128 + r]);
+        const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+        if (row_ok) {
+          uint8_t* q = static_cast<uint8_t*>(args.out) + (int64_t)(tc.out_row + r) * args.out_ld + tc.n_idx * 128 +
+                       half * 64;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            uint4 pk;
+            uint32_t* p32 = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int i = w * 16 + j * 4;
+              const uint32_t lo = e4m3x2(acc[i] / scale, acc[i + 1] / scale);
+              const uint32_t hi = e4m3x2(acc[i + 2] / scale, acc[i + 3] / scale);
+              p32[j] = lo | (hi << 16);
+            }
+            reinterpret_cast<uint4*>(q)[w] = pk;
+          }
+          if (half == 0) args.out_scale[(int64_t)tc.n_idx * args.out_scale_ld + tc.out_row + r] = scale;
+        }
+      } else {
+        if (row_ok && half_ok) {
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(args.out) + (int64_t)(tc.out_row + r) * args.out_ld +
+                             tc.n_idx * BN + half * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = acc[c * 32 + i];
+            store_bf16x32(o + c * 32, v);
+          }
+        }
+      }
+    }
+    if (!ok) *abort_flag = 1;
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+}  // namespace moe

@@ -17,12 +17,14 @@ namespace moe {
 // ---------------------------------------------------------------------------
 // Router top-k (ai.flicky.cc 2.1.2, the g'_{i,t} rule; xyznot.com Method 2).
 // One warp per token.  Lane l holds experts l, l+32, ... (VPL of them):
-// s = sigmoid(z), score = s + b.  k rounds of a warp arg-max (score
+// z = the sum of the logits GEMM's K splits in split order, s = sigmoid(z),
+// score = s + b.  k rounds of a warp arg-max (score
 // descending, ties to the lower index) pick the experts; the gates are the
 // selected unbiased s divided by their sum.  Lane j keeps the j-th pick.
 // A NaN score ranks as -inf.
 template <int VPL>
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ z, int T, int E, int k,
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ z, int splits,
+                                                         int64_t split_stride, int T, int E, int k,
                                                          const float* __restrict__ bias, int32_t* __restrict__ idx_out,
                                                          float* __restrict__ gate_out, int32_t* __restrict__ counts,
                                                          uint32_t* __restrict__ mask, int W) {
@@ -35,7 +37,9 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   for (int j = 0; j < VPL; ++j) {
     const int e = lane + 32 * j;
     if (e < E) {
-      const float s = 1.0f / (1.0f + expf(-z[(int64_t)t * E + e]));
+      float zz = z[(int64_t)t * E + e];
+      for (int p = 1; p < splits; ++p) zz += z[p * split_stride + (int64_t)t * E + e];
+      const float s = 1.0f / (1.0f + expf(-zz));
       float score = s + bias[e];
       if (isnan(score)) score = -INFINITY;
       sc[j] = score;
@@ -154,13 +158,16 @@ __global__ void __launch_bounds__(256) expert_scan_kernel(const uint32_t* __rest
 }
 
 // One block (1024 threads): row offsets of the experts and the GEMM group
-// table (128-row tiles per expert, prefix of tiles).  With clamp_rows >= 0
-// the counts come from untrusted offsets (moe_grouped_ffn): they are made
-// non-decreasing and clipped to [0, clamp_rows], flagging any repair.
+// table (chunks of `chunk` rows per expert, prefix of chunks).  With
+// offs_in != nullptr the counts come from untrusted offsets
+// (moe_grouped_ffn): they are made non-decreasing and clipped to
+// [0, clamp_rows], flagging any repair.
+// chunk_group (optional, cg_cap entries) receives the group of every chunk,
+// so a GEMM maps a chunk index to its group with one load.
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ cnt, const int32_t* __restrict__ offs_in,
-                                                    int G, int clamp_rows, int32_t* __restrict__ offsets_out,
+                                                    int G, int clamp_rows, int chunk, int32_t* __restrict__ offsets_out,
                                                     GroupEntry* __restrict__ groups, int32_t* __restrict__ mt_total,
-                                                    int* status) {
+                                                    int32_t* __restrict__ chunk_group, int cg_cap, int* status) {
   __shared__ int warp_sums[32];
   __shared__ int carry_rows, carry_mt;
   if (threadIdx.x == 0) {
@@ -182,7 +189,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
         rows = cnt[g];
       }
     }
-    const int mt = (rows + 127) / 128;
+    const int mt = (rows + chunk - 1) / chunk;
     int tot_rows, tot_mt;
     const int ex_rows = block_exclusive_scan(rows, warp_sums, tot_rows);
     const int ex_mt = block_exclusive_scan(mt, warp_sums, tot_mt);
@@ -190,6 +197,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
       const int off = offs_in ? a0 : carry_rows + ex_rows;
       if (offsets_out) offsets_out[g] = off;
       groups[g] = GroupEntry{off, off, rows, carry_mt + ex_mt};
+      if (chunk_group)
+        for (int j = carry_mt + ex_mt; j < carry_mt + ex_mt + mt && j < cg_cap; ++j) chunk_group[j] = g;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -200,7 +209,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
   }
   if (threadIdx.x == 0) {
     if (offsets_out) offsets_out[G] = carry_rows;
-    *mt_total = carry_mt;
+    if (chunk_group && carry_mt > cg_cap) record_status(status, ST_BAD_INDEX);  // overlapping untrusted offsets
+    *mt_total = chunk_group ? min(carry_mt, cg_cap) : carry_mt;
   }
 }
 

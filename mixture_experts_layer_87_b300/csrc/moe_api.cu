@@ -13,6 +13,8 @@
 #include <cstring>
 #include <mutex>
 
+#include "expert_gemm.cuh"
+#include "fp8_gemm.cuh"
 #include "kernels.cuh"
 #include "moe.h"
 
@@ -23,9 +25,37 @@ namespace {
 constexpr size_t kAlign = 256;
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
+// Entries of the chunk -> group table: at most rows/128 + one partial chunk
+// per group (chunks are >= 128 rows).
+int64_t cgroup_cap(const moe_dims& d) {
+  return (int64_t(d.T) * d.k + 127) / 128 + d.E + d.n_shared + 1;
+}
+
+// K splits of the router logits GEMM: more CTAs for the centroid stream when
+// there are few tokens (up to the 148 SMs of a B300, at most 8 splits), at
+// most 2^21 fp32 partial logits in all (the scratch of moe_route_noalloc
+// holds that many).
+struct LogitsSplit {
+  int splits, kb_per_split;
+};
+
+LogitsSplit logits_split(const moe_dims& d) {
+  const int64_t tiles = ((int64_t(d.T) + 127) / 128) * ((int64_t(d.E) + 127) / 128);
+  const int num_kb = (d.d + 63) / 64;
+  // at most 8 splits: the top-k kernel reads every split's partial logits
+  int64_t want = tiles > 0 ? 148 / tiles : 1;
+  if (want > 8) want = 8;
+  const int64_t te = int64_t(d.T) * d.E;
+  if (te > 0 && want * te > MOE_ROUTE_NOALLOC_MAX_LOGITS) want = MOE_ROUTE_NOALLOC_MAX_LOGITS / te;
+  if (want < 1) want = 1;
+  if (want > num_kb) want = num_kb;
+  const int kb_per = static_cast<int>((num_kb + want - 1) / want);
+  return LogitsSplit{(num_kb + kb_per - 1) / kb_per, kb_per};
+}
+
 // Byte offsets of every buffer inside the caller's workspace.
 struct Layout {
-  size_t status, z, idx, gate, counts, mask, wprefix, cnt, offsets, groups, mt_total, perm, slot;
+  size_t status, queue, z, idx, gate, counts, mask, wprefix, cnt, offsets, groups, mt_total, cgroup, perm, slot;
   size_t x, xs, uq, uqs, h, hs, hsh, hshs, y, ysh, total;
 };
 
@@ -41,7 +71,8 @@ Layout make_layout(const moe_dims& d) {
   const bool fp8 = d.prec == MOE_FP8_E4M3;
   const int64_t eb = fp8 ? 1 : 2;  // bytes per GEMM operand element
   L.status = take(256);
-  L.z = take(T * E * 4);
+  L.queue = take(4 * sizeof(int));  // item counters of the four expert GEMM launches
+  L.z = take(logits_split(d).splits * T * E * 4);
   L.idx = take(R * 4);
   L.gate = take(R * 4);
   L.counts = take(E * 4);
@@ -51,6 +82,7 @@ Layout make_layout(const moe_dims& d) {
   L.offsets = take((E + 1) * 4);
   L.groups = take((E + Ns + 1) * sizeof(GroupEntry));
   L.mt_total = take(16);
+  L.cgroup = take(cgroup_cap(d) * 4);
   L.perm = take(R * 4);
   L.slot = take(R * 4);
   L.x = take(R * D * eb);
@@ -141,18 +173,6 @@ moe_status make_tmap(CUtensorMap* map, const void* base, bool fp8, int64_t rows,
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
-template <bool FP8, int BN, Epi EPI>
-moe_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int64_t grid,
-                       cudaStream_t st) {
-  if (grid <= 0) return MOE_OK;
-  if (grid > INT_MAX) return MOE_ERR_UNSUPPORTED;
-  constexpr size_t smem = gemm_smem_bytes<FP8, BN>();
-  auto kern = grouped_gemm_kernel<FP8, BN, EPI>;
-  MOE_TRY(cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))));
-  kern<<<static_cast<unsigned>(grid), GemmShape<FP8>::THREADS, smem, st>>>(ta, tb, a);
-  return launched();
-}
-
 GemmArgs base_args(int* status) {
   GemmArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -162,8 +182,10 @@ GemmArgs base_args(int* status) {
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Upper bound of the 128-row tiles of `groups` groups holding `rows` rows.
-int64_t mt_bound(int64_t rows, int64_t groups) { return cdiv(rows + 127 * groups, 128); }
+// Token rows per chunk of the expert GEMMs (the N of one MMA at most).
+constexpr int kChunkBf16 = kXChunk;
+constexpr int kChunkFp8 = 128;
+int chunk_rows(const moe_dims& d) { return d.prec == MOE_FP8_E4M3 ? kChunkFp8 : kChunkBf16; }
 
 // ------------------------------------------------------------------ pieces
 // Router logits (tcgen05 GEMM, bf16 in, fp32 out) then the warp-per-token top-k.
@@ -172,23 +194,31 @@ moe_status enqueue_route(const moe_dims& d, const uint16_t* u, const uint16_t* c
                          Recorder* rec = nullptr) {
   const int W = (d.T + 31) / 32;
   MOE_TRY(cuda_ok(cudaMemsetAsync(counts, 0, sizeof(int32_t) * d.E, st)));
-  CUtensorMap ta, tb;
-  MOE_TRY(make_tmap(&ta, u, false, d.T, d.d, 128));
-  MOE_TRY(make_tmap(&tb, cent, false, d.E, d.d, 128));
-  GemmArgs a = base_args(status);
-  a.n_groups = 1;
-  a.uni_m = d.T;
-  a.N = d.E;
+  CUtensorMap tu, tc;
+  MOE_TRY(make_tmap(&tu, u, false, d.T, d.d, 128));
+  MOE_TRY(make_tmap(&tc, cent, false, d.E, d.d, 128));
+  const LogitsSplit sp = logits_split(d);
+  LogitsArgs a;
+  a.T = d.T;
+  a.E = d.E;
   a.K = d.d;
-  a.b_rows_per_group = d.E;
-  a.a_rows_cap = d.T;
-  a.out = z;
-  a.out_ld = d.E;
-  MOE_TRY((launch_gemm<false, 128, Epi::F32>(ta, tb, a, cdiv(d.T, 128) * cdiv(d.E, 128), st)));
+  a.kb_per_split = sp.kb_per_split;
+  a.z = z;
+  a.split_stride = int64_t(d.T) * d.E;
+  a.status = status;
+  const int64_t grid = cdiv(d.T, 128) * cdiv(d.E, 128) * sp.splits;
+  if (grid > INT_MAX) return MOE_ERR_UNSUPPORTED;
+  constexpr size_t smem = logits_smem_bytes();
+  MOE_TRY(cuda_ok(cudaFuncSetAttribute(logits_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem))));
+  logits_gemm_kernel<<<static_cast<unsigned>(grid), 192, smem, st>>>(tu, tc, a);
+  MOE_TRY(launched());
   if (rec) MOE_TRY(rec->mark());
   const unsigned blocks = static_cast<unsigned>(cdiv(int64_t(d.T) * 32, 256));
   const int vpl = (d.E + 31) / 32;
-#define MOE_TOPK(V) route_topk_kernel<V><<<blocks, 256, 0, st>>>(z, d.T, d.E, d.k, bias, idx, gate, counts, mask, W)
+#define MOE_TOPK(V)                                                                                              \
+  route_topk_kernel<V><<<blocks, 256, 0, st>>>(z, sp.splits, a.split_stride, d.T, d.E, d.k, bias, idx, gate, counts, \
+                                               mask, W)
   if (vpl <= 1) MOE_TOPK(1);
   else if (vpl <= 2) MOE_TOPK(2);
   else if (vpl <= 4) MOE_TOPK(4);
@@ -204,12 +234,13 @@ moe_status enqueue_route(const moe_dims& d, const uint16_t* u, const uint16_t* c
 // table, and the gather of permuted rows (FP8: quantised on the way).
 moe_status enqueue_dispatch(const moe_dims& d, const int32_t* idx, const uint16_t* u, const uint32_t* mask,
                             int32_t* wprefix, int32_t* cnt, int32_t* offsets, GroupEntry* groups, int32_t* mt_total,
-                            int32_t* perm, int32_t* slot, void* x, float* xs, uint8_t* uq, float* uqs, int* status,
+                            int32_t* cgroup, int32_t* perm, int32_t* slot, void* x, float* xs, uint8_t* uq, float* uqs, int* status,
                             cudaStream_t st, Recorder* rec = nullptr) {
   const int W = (d.T + 31) / 32;
   expert_scan_kernel<<<d.E, 256, 0, st>>>(mask, W, wprefix, cnt);
   MOE_TRY(launched());
-  plan_kernel<<<1, 1024, 0, st>>>(cnt, nullptr, d.E, 0, offsets, groups, mt_total, status);
+  plan_kernel<<<1, 1024, 0, st>>>(cnt, nullptr, d.E, 0, chunk_rows(d), offsets, groups, mt_total, cgroup,
+                                  static_cast<int>(cgroup_cap(d)), status);
   MOE_TRY(launched());
   if (rec) MOE_TRY(rec->mark());
   const unsigned blocks = static_cast<unsigned>(cdiv(int64_t(d.T) * 32, 256));
@@ -225,11 +256,56 @@ moe_status enqueue_dispatch(const moe_dims& d, const int32_t* idx, const uint16_
   return rec ? rec->mark() : MOE_OK;
 }
 
+// Streaming multiprocessors of the current device (the persistent grid).
+moe_status sm_count(int* n) {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+    *n = cache[dev];
+    return MOE_OK;
+  }
+  int v = 0;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) return MOE_ERR_CUDA;
+  if (dev >= 0 && dev < 64) cache[dev] = v;
+  *n = v;
+  return MOE_OK;
+}
+
+template <Epi EPI>
+moe_status launch_xgemm(const CUtensorMap& tw, const CUtensorMap& tx, const XGemmArgs& a, int64_t items_bound,
+                        cudaStream_t st) {
+  if (items_bound <= 0) return MOE_OK;
+  int sms = 0;
+  MOE_TRY(sm_count(&sms));
+  const int64_t grid = items_bound < sms ? items_bound : sms;
+  constexpr size_t smem = xgemm_smem_bytes();
+  auto kern = expert_gemm_kernel<EPI>;
+  MOE_TRY(cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))));
+  kern<<<static_cast<unsigned>(grid), kXThreads, smem, st>>>(tw, tx, a);
+  return launched();
+}
+
+template <Epi EPI>
+moe_status launch_fp8(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int64_t items_bound,
+                      cudaStream_t st) {
+  if (items_bound <= 0) return MOE_OK;
+  int sms = 0;
+  MOE_TRY(sm_count(&sms));
+  const int64_t grid = items_bound < sms ? items_bound : sms;
+  constexpr size_t smem = fp8_gemm_smem_bytes();
+  auto kern = fp8_gemm_kernel<EPI>;
+  MOE_TRY(cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))));
+  kern<<<static_cast<unsigned>(grid), F8Shape::THREADS, smem, st>>>(ta, tb, a);
+  return launched();
+}
+
 // Gate/up (+SwiGLU) then down GEMMs over a set of groups.
-//   table != nullptr: routed experts, rows from the device table (upper bound
-//   rows_cap rows over n_groups groups).  Otherwise n_groups uniform groups of
-//   uni_m rows each; gate/up A rows start at 0 for every group (all shared
-//   experts read the same tokens).
+//   table != nullptr: routed experts, rows from the device table (chunk
+//   counts from plan_kernel with chunk_rows(d); upper bound rows_cap rows over
+//   n_groups groups).  Otherwise n_groups uniform groups of uni_m rows each;
+//   gate/up X rows start at 0 for every group (all shared experts read the
+//   same tokens).
 struct FfnOperands {
   const void* x;
   const float* xs;
@@ -244,20 +320,24 @@ struct FfnOperands {
   int64_t rows_cap;  // rows allocated in h and y
 };
 
-moe_status enqueue_ffn(const moe_dims& d, const FfnOperands& o, int n_groups, const GroupEntry* table,
-                       const int32_t* mt_total, int uni_m, int* status, cudaStream_t st, Recorder* rec = nullptr) {
-  const bool fp8 = d.prec == MOE_FP8_E4M3;
+// FP8: tokens on the 128 TMEM lanes (128-row tiles of grouped_gemm_kernel),
+// so the promotion scale of a lane is one activation scale per k-block.
+moe_status enqueue_ffn_fp8(const moe_dims& d, const FfnOperands& o, int n_groups, const GroupEntry* table,
+                           const int32_t* mt_total, const int32_t* cgroup, int uni_m, int* queue, int* status,
+                           cudaStream_t st, Recorder* rec) {
   const int I = d.inter, D = d.d;
   CUtensorMap ta1, tb1, ta2, tb2;
-  MOE_TRY(make_tmap(&ta1, o.x, fp8, o.x_rows, D, 128));
-  MOE_TRY(make_tmap(&tb1, o.w13, fp8, int64_t(n_groups) * 2 * I, D, 256));
-  MOE_TRY(make_tmap(&ta2, o.h, fp8, o.rows_cap, I, 128));
-  MOE_TRY(make_tmap(&tb2, o.w2, fp8, int64_t(n_groups) * D, I, 256));
-  const int64_t mt = table ? mt_bound(o.rows_cap, n_groups) : int64_t(n_groups) * cdiv(uni_m, 128);
+  MOE_TRY(make_tmap(&ta1, o.x, true, o.x_rows, D, 128));
+  MOE_TRY(make_tmap(&tb1, o.w13, true, int64_t(n_groups) * 2 * I, D, 256));
+  MOE_TRY(make_tmap(&ta2, o.h, true, o.rows_cap, I, 128));
+  MOE_TRY(make_tmap(&tb2, o.w2, true, int64_t(n_groups) * D, I, 256));
+  const int64_t mt = table ? cdiv(o.rows_cap + 127 * int64_t(n_groups), 128) : int64_t(n_groups) * cdiv(uni_m, 128);
 
   GemmArgs a = base_args(status);
+  a.queue = queue;
   a.groups = table;
   a.mt_total = mt_total;
+  a.chunk_group = cgroup;
   a.n_groups = n_groups;
   a.uni_m = uni_m;
   a.uni_a_step = 0;
@@ -273,12 +353,11 @@ moe_status enqueue_ffn(const moe_dims& d, const FfnOperands& o, int n_groups, co
   a.b_scale = o.w13s;
   a.out_scale = o.hs;
   a.out_scale_ld = o.rows_cap;
-  const int64_t g1 = mt * (2 * I / 256);
-  if (fp8) MOE_TRY((launch_gemm<true, 256, Epi::SWIGLU>(ta1, tb1, a, g1, st)));
-  else MOE_TRY((launch_gemm<false, 256, Epi::SWIGLU>(ta1, tb1, a, g1, st)));
+  MOE_TRY((launch_fp8<Epi::SWIGLU>(ta1, tb1, a, mt * (2 * I / 256), st)));
   if (rec) MOE_TRY(rec->mark());
 
   GemmArgs b = a;
+  b.queue = queue + 1;
   b.uni_a_step = uni_m;
   b.N = D;
   b.K = I;
@@ -290,9 +369,56 @@ moe_status enqueue_ffn(const moe_dims& d, const FfnOperands& o, int n_groups, co
   b.a_scale_ld = o.rows_cap;
   b.b_scale = o.w2s;
   b.out_scale = nullptr;
-  const int64_t g2 = mt * cdiv(D, 256);
-  if (fp8) MOE_TRY((launch_gemm<true, 256, Epi::BF16>(ta2, tb2, b, g2, st)));
-  else MOE_TRY((launch_gemm<false, 256, Epi::BF16>(ta2, tb2, b, g2, st)));
+  MOE_TRY((launch_fp8<Epi::BF16>(ta2, tb2, b, mt * cdiv(D, 256), st)));
+  return rec ? rec->mark() : MOE_OK;
+}
+
+// bf16: weights on the TMEM lanes, tokens on the columns (expert_gemm_kernel).
+// queue: two zeroed item counters (gate/up launch, down launch).
+moe_status enqueue_ffn(const moe_dims& d, const FfnOperands& o, int n_groups, const GroupEntry* table,
+                       const int32_t* ch_total, const int32_t* cgroup, int uni_m, int* queue, int* status,
+                       cudaStream_t st, Recorder* rec = nullptr) {
+  if (d.prec == MOE_FP8_E4M3)
+    return enqueue_ffn_fp8(d, o, n_groups, table, ch_total, cgroup, uni_m, queue, status, st, rec);
+  const int I = d.inter, D = d.d;
+  constexpr int CH = kChunkBf16;
+  CUtensorMap tx1, tw1, tx2, tw2;
+  MOE_TRY(make_tmap(&tx1, o.x, false, o.x_rows, D, CH));
+  MOE_TRY(make_tmap(&tw1, o.w13, false, int64_t(n_groups) * 2 * I, D, 256));
+  MOE_TRY(make_tmap(&tx2, o.h, false, o.rows_cap, I, CH));
+  MOE_TRY(make_tmap(&tw2, o.w2, false, int64_t(n_groups) * D, I, 256));
+  // upper bound of the token chunks: every group adds at most one partial chunk
+  const int64_t chunks = table ? cdiv(o.rows_cap + int64_t(CH - 1) * n_groups, CH)
+                               : int64_t(n_groups) * cdiv(uni_m, CH);
+
+  XGemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.status = status;
+  a.queue = queue;
+  a.groups = table;
+  a.ch_total = ch_total;
+  a.chunk_group = cgroup;
+  a.n_groups = n_groups;
+  a.uni_m = uni_m;
+  a.uni_a_step = 0;
+  a.uni_out_step = uni_m;
+  a.Nw = 2 * I;
+  a.K = D;
+  a.x_rows = static_cast<int32_t>(o.x_rows);
+  a.out = o.h;
+  a.out_ld = I;
+  MOE_TRY((launch_xgemm<Epi::SWIGLU>(tw1, tx1, a, chunks * cdiv(2 * I, 256), st)));
+  if (rec) MOE_TRY(rec->mark());
+
+  XGemmArgs b = a;
+  b.queue = queue + 1;
+  b.uni_a_step = uni_m;
+  b.Nw = D;
+  b.K = I;
+  b.x_rows = static_cast<int32_t>(o.rows_cap);
+  b.out = o.y;
+  b.out_ld = D;
+  MOE_TRY((launch_xgemm<Epi::BF16>(tw2, tx2, b, chunks * cdiv(D, 256), st)));
   return rec ? rec->mark() : MOE_OK;
 }
 
@@ -368,8 +494,8 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, const uint
     MOE_TRY(launched());
   }
   return enqueue_dispatch(*dims, topk_idx, u, mask, at<int32_t>(ws, L.wprefix), at<int32_t>(ws, L.cnt), offsets,
-                          at<GroupEntry>(ws, L.groups), at<int32_t>(ws, L.mt_total), perm, slot, x_perm, x_scale,
-                          nullptr, nullptr, status, st);
+                          at<GroupEntry>(ws, L.groups), at<int32_t>(ws, L.mt_total), at<int32_t>(ws, L.cgroup), perm,
+                          slot, x_perm, x_scale, nullptr, nullptr, status, st);
 }
 
 moe_status moe_grouped_ffn(const moe_dims* dims, int32_t n_groups, int32_t rows, const int32_t* offsets,
@@ -391,11 +517,15 @@ moe_status moe_grouped_ffn(const moe_dims* dims, int32_t n_groups, int32_t rows,
   if (rows == 0) return MOE_OK;
   GroupEntry* groups = at<GroupEntry>(ws, L.groups);
   int32_t* mt_total = at<int32_t>(ws, L.mt_total);
-  plan_kernel<<<1, 1024, 0, st>>>(nullptr, offsets, n_groups, rows, nullptr, groups, mt_total, status);
+  int32_t* cgroup = at<int32_t>(ws, L.cgroup);
+  int* queue = at<int>(ws, L.queue);
+  MOE_TRY(cuda_ok(cudaMemsetAsync(queue, 0, 2 * sizeof(int), st)));
+  plan_kernel<<<1, 1024, 0, st>>>(nullptr, offsets, n_groups, rows, chunk_rows(*dims), nullptr, groups, mt_total,
+                                  cgroup, static_cast<int>(cgroup_cap(*dims)), status);
   MOE_TRY(launched());
   FfnOperands o{x, x_scale, rows, w13, w13_scale, w2, w2_scale, at<void>(ws, L.h),
                 fp8 ? at<float>(ws, L.hs) : nullptr, y, rows};
-  return enqueue_ffn(*dims, o, n_groups, groups, mt_total, 0, status, st);
+  return enqueue_ffn(*dims, o, n_groups, groups, mt_total, cgroup, 0, queue, status, st);
 }
 
 moe_status moe_combine(const moe_dims* dims, const uint16_t* u, const uint16_t* shared_y, const uint16_t* y_perm,
@@ -445,7 +575,8 @@ moe_status moe_forward_profiled(const moe_dims* dims, const moe_weights* w, cons
   Recorder* rec = events ? &recorder : nullptr;
   if (rec) MOE_TRY(rec->mark());
   int* status = at<int>(ws, L.status);
-  MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, sizeof(int), st)));
+  int* queue = at<int>(ws, L.queue);
+  MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, L.queue + 4 * sizeof(int), st)));  // status word and item counters
   int32_t* counts = counts_out ? counts_out : at<int32_t>(ws, L.counts);
   if (d.T == 0) return cuda_ok(cudaMemsetAsync(counts, 0, sizeof(int32_t) * d.E, st));
   const int W = (d.T + 31) / 32;
@@ -461,7 +592,8 @@ moe_status moe_forward_profiled(const moe_dims* dims, const moe_weights* w, cons
   int32_t* slot = at<int32_t>(ws, L.slot);
   const int64_t R = int64_t(d.T) * d.k;
   MOE_TRY(enqueue_dispatch(d, idx, u, mask, at<int32_t>(ws, L.wprefix), at<int32_t>(ws, L.cnt),
-                           at<int32_t>(ws, L.offsets), groups, mt_total, at<int32_t>(ws, L.perm), slot,
+                           at<int32_t>(ws, L.offsets), groups, mt_total, at<int32_t>(ws, L.cgroup),
+                           at<int32_t>(ws, L.perm), slot,
                            at<void>(ws, L.x), fp8 ? at<float>(ws, L.xs) : nullptr,
                            fp8 ? at<uint8_t>(ws, L.uq) : nullptr, fp8 ? at<float>(ws, L.uqs) : nullptr, status, st,
                            rec));
@@ -469,7 +601,7 @@ moe_status moe_forward_profiled(const moe_dims* dims, const moe_weights* w, cons
   // routed experts: groups from the device table
   FfnOperands ro{at<void>(ws, L.x), fp8 ? at<float>(ws, L.xs) : nullptr, R, w->w13, w->w13_scale, w->w2,
                  w->w2_scale, at<void>(ws, L.h), fp8 ? at<float>(ws, L.hs) : nullptr, at<uint16_t>(ws, L.y), R};
-  MOE_TRY(enqueue_ffn(d, ro, d.E, groups, mt_total, 0, status, st, rec));
+  MOE_TRY(enqueue_ffn(d, ro, d.E, groups, mt_total, at<int32_t>(ws, L.cgroup), 0, queue, status, st, rec));
 
   // shared experts: every token, n_shared uniform groups
   uint16_t* ysh = at<uint16_t>(ws, L.ysh);
@@ -477,7 +609,7 @@ moe_status moe_forward_profiled(const moe_dims* dims, const moe_weights* w, cons
     const void* xa = fp8 ? static_cast<const void*>(at<uint8_t>(ws, L.uq)) : static_cast<const void*>(u);
     FfnOperands so{xa, fp8 ? at<float>(ws, L.uqs) : nullptr, d.T, w->ws13, w->ws13_scale, w->ws2, w->ws2_scale,
                    at<void>(ws, L.hsh), fp8 ? at<float>(ws, L.hshs) : nullptr, ysh, int64_t(d.n_shared) * d.T};
-    MOE_TRY(enqueue_ffn(d, so, d.n_shared, nullptr, nullptr, d.T, status, st, rec));
+    MOE_TRY(enqueue_ffn(d, so, d.n_shared, nullptr, nullptr, nullptr, d.T, queue + 2, status, st, rec));
   } else if (rec) {
     MOE_TRY(rec->mark());
     MOE_TRY(rec->mark());

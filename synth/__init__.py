@@ -132,6 +132,12 @@ CONFIGS = {
                           prec="fp8", rho=V3_RHO, alpha=V3_ALPHA),
     "decode": LayerConfig("decode", T=256, d=7168, E=256, k=8, n_shared=1, inter=2048,
                           prec="fp8", bias="zero", rho=V3_RHO, alpha=DECODE_ALPHA, steps=50),
+    # V3 expert shapes with 32 experts (mean 256 rows per expert, as at V3):
+    # the workload ncu captures, small enough to hold on the device many times.
+    "v3_slice": LayerConfig("v3_slice", T=1024, d=7168, E=32, k=8, n_shared=1, inter=2048,
+                            rho=V3_RHO, alpha=V3_ALPHA),
+    "v3_slice_fp8": LayerConfig("v3_slice_fp8", T=1024, d=7168, E=32, k=8, n_shared=1, inter=2048,
+                                prec="fp8", rho=V3_RHO, alpha=V3_ALPHA),
     # Small parity shapes: several M/N/K tiles, ragged tails, odd expert counts.
     "ragged": LayerConfig("ragged", T=300, d=384, E=20, k=3, n_shared=1, inter=256,
                           rho=0.3, alpha=1.0),
