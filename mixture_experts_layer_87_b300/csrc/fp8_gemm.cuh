@@ -14,11 +14,10 @@
 // and decodes them, see the item ring of expert_gemm.cuh).  Warp 0
 // issues TMA loads into a 4-stage ring (16 KB of tokens + 32 KB of weights
 // per 128-K stage), one thread of warp 1 issues kind::f8f6f4 MMAs (K = 32)
-// into one of two TMEM partial buffers (2 x 256 columns), warps 2..9 promote:
-// the warp of lane quarter q and column half c reads 16-column slices of the
-// partial (the next slice's tcgen05.ld in flight during the current FMAs),
-// multiplies by s_x * s_w and adds into 128 fp32 registers, then frees the
-// buffer for the MMA two K blocks ahead.  Warps whose 32 rows all lie past
+// into one of two TMEM partial buffers (2 x 256 columns), the epilogue warps
+// promote: each reads 16-column slices of its lane quarter's share of the
+// partial, multiplies by s_x * s_w and adds into fp32 registers (packed
+// fp32x2 FMAs), then frees the buffer for the MMA two K blocks ahead.  Warps whose 32 rows all lie past
 // the group's end keep the barrier phases in step without loading anything.
 //
 // Epilogues:
@@ -38,17 +37,27 @@
 
 namespace moe {
 
+// EW epilogue warps, EW / 4 per TMEM lane quarter.  8: 128 accumulators per
+// thread and a software-pipelined TMEM read; 16: 64 accumulators per thread,
+// twice the warps on a quarter -- the better choice when few rows per tile
+// are valid (a decode step: 8 tokens per expert on average) and all the
+// work falls on one quarter.
+template <int EW>
 struct F8Shape {
   static constexpr int BM = 128, BN = 256, BK = 128, UK = 32;
   static constexpr uint32_t A_BYTES = BM * 128, B_BYTES = BN * 128;
   static constexpr int STAGES = 4;
-  static constexpr int EPI_WARPS = 8;
-  static constexpr int THREADS = 32 * (3 + EPI_WARPS);  // producer, MMA, epilogue, scheduler
+  static constexpr int EPI_WARPS = EW;
+  static constexpr int CG = EW / 4;
+  static constexpr int THREADS = 32 * (3 + EW);  // producer, MMA, epilogue, scheduler
+  static_assert(CG == 2 || CG == 4, "column groups");
 };
 
+template <int EW>
 constexpr size_t fp8_gemm_smem_bytes() {
-  return 1024 + size_t(F8Shape::STAGES) * (F8Shape::A_BYTES + F8Shape::B_BYTES) + 512 /* barriers, item ring */ +
-         2 * 2 * 128 * sizeof(float) /* amax exchange: 2 items x 2 halves x 128 rows */;
+  using S = F8Shape<EW>;
+  return 1024 + size_t(S::STAGES) * (S::A_BYTES + S::B_BYTES) + 512 /* barriers, item ring */ +
+         2 * S::CG * 128 * sizeof(float) /* amax exchange: 2 items x CG column groups x 128 rows */;
 }
 
 // Item -> (group, column block, row tile); the same ordering and table as
@@ -81,11 +90,29 @@ __device__ __forceinline__ bool f8decode(const GemmArgs& a, int tile, int items,
   return true;
 }
 
-template <Epi EPI>
-__global__ void __launch_bounds__(F8Shape::THREADS, 1)
+// (a0, a1) += (v0, v1) * s as one packed fp32x2 FMA (each lane a correctly
+// rounded fp32 FMA, as fmaf).
+__device__ __forceinline__ void fma2(float& a0, float& a1, uint32_t v0, uint32_t v1, float s) {
+#if MOE_NO_F32X2
+  a0 = fmaf(__uint_as_float(v0), s, a0);
+  a1 = fmaf(__uint_as_float(v1), s, a1);
+#else
+  asm("{\n\t.reg .b64 acc, val, sc;\n\t"
+      "mov.b64 acc, {%0, %1};\n\t"
+      "mov.b64 val, {%2, %3};\n\t"
+      "mov.b64 sc, {%4, %4};\n\t"
+      "fma.rn.f32x2 acc, val, sc, acc;\n\t"
+      "mov.b64 {%0, %1}, acc;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "r"(v0), "r"(v1), "f"(s));
+#endif
+}
+
+template <Epi EPI, int EW>
+__global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmArgs args) {
-  using S = F8Shape;
+  using S = F8Shape<EW>;
   constexpr int BN = S::BN, STAGES = S::STAGES;
   constexpr uint32_t A_BYTES = S::A_BYTES, B_BYTES = S::B_BYTES;
   constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -99,15 +126,15 @@ __global__ void __launch_bounds__(F8Shape::THREADS, 1)
   uint64_t* empty = full + STAGES;
   uint64_t* acc_full = empty + STAGES;  // [2] partial buffer written
   uint64_t* acc_empty = acc_full + 2;   // [2] partial buffer drained (8 warps)
-  uint64_t* pair_bar = acc_empty + 2;   // [4] the two warps of one lane quarter
-  uint64_t* mma_done = pair_bar + 4;
+  uint64_t* quarter_bar = acc_empty + 2;  // [4] the CG warps of one lane quarter
+  uint64_t* mma_done = quarter_bar + 4;
   ItemRing ring;
   ring.q_full = mma_done + 1;
   ring.q_empty = ring.q_full + kQueueSlots;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ring.q_empty + kQueueSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   ring.slot = reinterpret_cast<int*>(tmem_slot + 4);
-  float* amax_x = reinterpret_cast<float*>(smem + STAGES * (A_BYTES + B_BYTES) + 512);  // [2][2][128]
+  float* amax_x = reinterpret_cast<float*>(smem + STAGES * (A_BYTES + B_BYTES) + 512);  // [2][CG][128]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = (args.N + BN - 1) / BN;
@@ -122,7 +149,7 @@ __global__ void __launch_bounds__(F8Shape::THREADS, 1)
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], S::EPI_WARPS);
     }
-    for (int q = 0; q < 4; ++q) mbar_init(&pair_bar[q], 2);
+    for (int q = 0; q < 4; ++q) mbar_init(&quarter_bar[q], S::CG);
     for (int q = 0; q < kQueueSlots; ++q) {
       mbar_init(&ring.q_full[q], 1);
       mbar_init(&ring.q_empty[q], 2 + S::EPI_WARPS);  // producer, MMA thread, epilogue warps
@@ -139,7 +166,7 @@ __global__ void __launch_bounds__(F8Shape::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 10) {
+  if (warp == 2 + S::EPI_WARPS) {
     // ------------------------------------------------------------ item scheduler
     if (lane == 0) {
       const int items = args.groups == nullptr ? (args.uni_m + 127) / 128 * nb * args.n_groups
@@ -215,13 +242,26 @@ __global__ void __launch_bounds__(F8Shape::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ promotion + epilogue
+    // The CG warps of one TMEM lane quarter split the 256 columns into CG
+    // groups of NCH 16-column chunks.  SWIGLU: a warp takes NCH/2 gate
+    // chunks of columns [0, 128) and the matching up chunks of [128, 256)
+    // (gate feature f and up feature f stay in one thread); plain: NCH
+    // consecutive chunks, all inside one 128-column weight block.
+    constexpr int CG = S::CG, NCH = 16 / CG, NP = NCH / 2;
     const int ew = warp - 2;
     const int quarter = warp & 3;  // TMEM lanes this warp may access
-    const int half = ew >> 2;      // SWIGLU: gate [64h, 64h+64) + up 128 + [64h, ..); plain: cols [128h, 128h+128)
+    const int cg = ew >> 2;
     const int r = quarter * 32 + lane;
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     const int KB = args.K / 128;
-    uint32_t it = 0, pphase = 0;
+    auto col_of = [&](int j) -> uint32_t {
+      if constexpr (EPI == Epi::SWIGLU)
+        return j < NP ? (cg * NP + j) * 16 : 128 + (cg * NP + j - NP) * 16;
+      else
+        return (cg * NCH + j) * 16;
+    };
+    const int blk = EPI == Epi::SWIGLU ? 0 : (cg * NCH * 16) / 128;  // plain: weight block of my columns
+    uint32_t it = 0, qphase = 0;
     bool ok = true;
     for (uint32_t lt = 0;; ++lt) {
       int v[6];
@@ -238,46 +278,55 @@ __global__ void __launch_bounds__(F8Shape::THREADS, 1)
       const float* sa_ptr = args.a_scale + a_row;
       const int b_row = tc.g * args.b_rows_per_group + tc.n_idx * BN;
       const float* sb_ptr = args.b_scale + (int64_t)(b_row / 128) * KB;
-      const bool half_ok = EPI == Epi::SWIGLU || tc.n_idx * BN + half * 128 < args.N;
-      const float* sb0_ptr = sb_ptr + (EPI == Epi::SWIGLU ? 0 : (int64_t)half * KB);
-      const float* sb1_ptr = sb_ptr + (EPI == Epi::SWIGLU ? KB : (int64_t)half * KB);
+      const bool blk_ok = EPI == Epi::SWIGLU || tc.n_idx * BN + blk * 128 < args.N;
+      const float* sb0_ptr = sb_ptr + (int64_t)blk * KB;                          // gate / my block
+      const float* sb1_ptr = sb_ptr + (EPI == Epi::SWIGLU ? KB : (int64_t)blk * KB);  // up / my block
       float sa_next = a_in ? __ldg(sa_ptr) : 0.0f;
-      float sb0_next = half_ok ? __ldg(sb0_ptr) : 0.0f, sb1_next = half_ok ? __ldg(sb1_ptr) : 0.0f;
-      float acc[128];
+      float sb0_next = blk_ok ? __ldg(sb0_ptr) : 0.0f, sb1_next = blk_ok ? __ldg(sb1_ptr) : 0.0f;
+      float acc[NCH * 16];
 #pragma unroll
-      for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+      for (int i = 0; i < NCH * 16; ++i) acc[i] = 0.0f;
 #pragma unroll 1
       for (int kb = 0; kb < num_kb; ++kb, ++it) {
         const uint32_t b = it & 1, u = it >> 1;
         const float s0 = sa_next * sb0_next, s1 = sa_next * sb1_next;
         if (kb + 1 < num_kb) {  // scales one K block ahead
           sa_next = a_in ? __ldg(sa_ptr + (int64_t)(kb + 1) * args.a_scale_ld) : 0.0f;
-          sb0_next = half_ok ? __ldg(sb0_ptr + kb + 1) : 0.0f;
-          sb1_next = half_ok ? __ldg(sb1_ptr + kb + 1) : 0.0f;
+          sb0_next = blk_ok ? __ldg(sb0_ptr + kb + 1) : 0.0f;
+          sb1_next = blk_ok ? __ldg(sb1_ptr + kb + 1) : 0.0f;
         }
         ok = __all_sync(0xffffffffu, xwait(&acc_full[b], u & 1, args.status, abort_flag));
         if (!ok) break;
         tc_fence_after();
         const uint32_t tb = t_lane + b * BN;
         if (warp_rows) {
-          auto col_of = [&](int j) -> uint32_t {
-            if constexpr (EPI == Epi::SWIGLU)
-              return j < 4 ? half * 64 + j * 16 : 128 + half * 64 + (j - 4) * 16;
-            else
-              return half * 128 + j * 16;
-          };
-          uint32_t va[16], vb[16];
-          tmem_ld16_nowait(tb + col_of(0), va);
-          tmem_ld_wait(va);
+          if constexpr (CG == 2) {
+            // the load of chunk j + 1 is in flight while the FMAs of chunk j run
+            uint32_t va[16], vb[16];
+            tmem_ld16_nowait(tb + col_of(0), va);
+            tmem_ld_wait(va);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            uint32_t(&cur)[16] = (j & 1) ? vb : va;
-            uint32_t(&nxt)[16] = (j & 1) ? va : vb;
-            if (j + 1 < 8) tmem_ld16_nowait(tb + col_of(j + 1), nxt);
-            const float sc = (EPI == Epi::SWIGLU && j >= 4) ? s1 : s0;
+            for (int j = 0; j < NCH; ++j) {
+              uint32_t(&cur)[16] = (j & 1) ? vb : va;
+              uint32_t(&nxt)[16] = (j & 1) ? va : vb;
+              if (j + 1 < NCH) tmem_ld16_nowait(tb + col_of(j + 1), nxt);
+              const float sc = (EPI == Epi::SWIGLU && j >= NP) ? s1 : s0;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[j * 16 + i] = fmaf(__uint_as_float(cur[i]), sc, acc[j * 16 + i]);
-            if (j + 1 < 8) tmem_ld_wait(nxt);
+              for (int i = 0; i < 16; i += 2) fma2(acc[j * 16 + i], acc[j * 16 + i + 1], cur[i], cur[i + 1], sc);
+              if (j + 1 < NCH) tmem_ld_wait(nxt);
+            }
+          } else {
+            // registers allow one chunk at a time; the other warps of the
+            // scheduler hide the load latency
+#pragma unroll
+            for (int j = 0; j < NCH; ++j) {
+              uint32_t cur[16];
+              tmem_ld16_nowait(tb + col_of(j), cur);
+              tmem_ld_wait(cur);
+              const float sc = (EPI == Epi::SWIGLU && j >= NP) ? s1 : s0;
+#pragma unroll
+              for (int i = 0; i < 16; i += 2) fma2(acc[j * 16 + i], acc[j * 16 + i + 1], cur[i], cur[i + 1], sc);
+            }
           }
         }
         tc_fence_before();
@@ -286,48 +335,52 @@ __global__ void __launch_bounds__(F8Shape::THREADS, 1)
       }
       if (!ok) break;
       if constexpr (EPI == Epi::SWIGLU) {
-        // h = SiLU(gate) * up for my 64 features; the row's 1 x 128 scale needs
-        // the partner warp's (other column half) amax as well.
+        // h = SiLU(gate) * up for my NP * 16 features; the row's 1 x 128 scale
+        // needs the amax of the other CG - 1 warps of the quarter too.
         float amax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          acc[i] = silu(acc[i]) * acc[64 + i];
+        for (int i = 0; i < NP * 16; ++i) {
+          acc[i] = silu(acc[i]) * acc[NP * 16 + i];
           amax = fmaxf(amax, fabsf(acc[i]));
         }
-        float* ax = amax_x + (lt & 1) * 256;  // alternate slots: the partner may still read the last item's
-        ax[half * 128 + r] = amax;
-        ok = group_sync(&pair_bar[quarter], pphase, args.status, abort_flag);
+        float* ax = amax_x + (lt & 1) * CG * 128;  // alternate slots: a partner may still read the last item's
+        ax[cg * 128 + r] = amax;
+        ok = group_sync(&quarter_bar[quarter], qphase, args.status, abort_flag);
         if (!ok) break;
-        amax = fmaxf(amax, ax[(half ^ 1) * 128 + r]);
+#pragma unroll
+        for (int c = 0; c < CG; ++c) amax = fmaxf(amax, ax[c * 128 + r]);
         const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+        // h is a GEMM output known to fp32 accuracy: its codes are taken from
+        // h * (1/scale), one correctly rounded reciprocal per row
+        const float inv = 1.0f / scale;
         if (row_ok) {
           uint8_t* q = static_cast<uint8_t*>(args.out) + (int64_t)(tc.out_row + r) * args.out_ld + tc.n_idx * 128 +
-                       half * 64;
+                       cg * NP * 16;
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
+          for (int w = 0; w < NP; ++w) {
             uint4 pk;
             uint32_t* p32 = reinterpret_cast<uint32_t*>(&pk);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const int i = w * 16 + j * 4;
-              const uint32_t lo = e4m3x2(acc[i] / scale, acc[i + 1] / scale);
-              const uint32_t hi = e4m3x2(acc[i + 2] / scale, acc[i + 3] / scale);
+              const uint32_t lo = e4m3x2(acc[i] * inv, acc[i + 1] * inv);
+              const uint32_t hi = e4m3x2(acc[i + 2] * inv, acc[i + 3] * inv);
               p32[j] = lo | (hi << 16);
             }
             reinterpret_cast<uint4*>(q)[w] = pk;
           }
-          if (half == 0) args.out_scale[(int64_t)tc.n_idx * args.out_scale_ld + tc.out_row + r] = scale;
+          if (cg == 0) args.out_scale[(int64_t)tc.n_idx * args.out_scale_ld + tc.out_row + r] = scale;
         }
       } else {
-        if (row_ok && half_ok) {
+        if (row_ok && blk_ok) {
           __nv_bfloat16* o = static_cast<__nv_bfloat16*>(args.out) + (int64_t)(tc.out_row + r) * args.out_ld +
-                             tc.n_idx * BN + half * 128;
+                             tc.n_idx * BN + cg * NCH * 16;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float v[32];
+          for (int c = 0; c < NCH / 2; ++c) {
+            float vv[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = acc[c * 32 + i];
-            store_bf16x32(o + c * 32, v);
+            for (int i = 0; i < 32; ++i) vv[i] = acc[c * 32 + i];
+            store_bf16x32(o + c * 32, vv);
           }
         }
       }

@@ -57,7 +57,10 @@ struct TileCoord {
   int32_t g, m_idx, n_idx, a_row, out_row, rows_valid;
 };
 
-__device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }
+// SiLU(x) = x * sigmoid(x), with the fast reciprocal division (its result is
+// rounded to bf16 or quantised to E4M3 next; for x -> -inf the denominator
+// overflows and the quotient is the correct limit 0).
+__device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);

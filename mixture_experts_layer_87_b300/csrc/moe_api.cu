@@ -286,18 +286,27 @@ moe_status launch_xgemm(const CUtensorMap& tw, const CUtensorMap& tx, const XGem
   return launched();
 }
 
+template <Epi EPI, int EW>
+moe_status launch_fp8_ew(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int64_t grid,
+                         cudaStream_t st) {
+  constexpr size_t smem = fp8_gemm_smem_bytes<EW>();
+  auto kern = fp8_gemm_kernel<EPI, EW>;
+  MOE_TRY(cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))));
+  kern<<<static_cast<unsigned>(grid), F8Shape<EW>::THREADS, smem, st>>>(ta, tb, a);
+  return launched();
+}
+
+// few_rows: most 128-row tiles hold few valid rows (fewer than 64 rows per
+// group on average), so the work sits on one TMEM lane quarter: 16 epilogue
+// warps share it.
 template <Epi EPI>
 moe_status launch_fp8(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int64_t items_bound,
-                      cudaStream_t st) {
+                      bool few_rows, cudaStream_t st) {
   if (items_bound <= 0) return MOE_OK;
   int sms = 0;
   MOE_TRY(sm_count(&sms));
   const int64_t grid = items_bound < sms ? items_bound : sms;
-  constexpr size_t smem = fp8_gemm_smem_bytes();
-  auto kern = fp8_gemm_kernel<EPI>;
-  MOE_TRY(cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))));
-  kern<<<static_cast<unsigned>(grid), F8Shape::THREADS, smem, st>>>(ta, tb, a);
-  return launched();
+  return few_rows ? launch_fp8_ew<EPI, 16>(ta, tb, a, grid, st) : launch_fp8_ew<EPI, 8>(ta, tb, a, grid, st);
 }
 
 // Gate/up (+SwiGLU) then down GEMMs over a set of groups.
@@ -353,7 +362,8 @@ moe_status enqueue_ffn_fp8(const moe_dims& d, const FfnOperands& o, int n_groups
   a.b_scale = o.w13s;
   a.out_scale = o.hs;
   a.out_scale_ld = o.rows_cap;
-  MOE_TRY((launch_fp8<Epi::SWIGLU>(ta1, tb1, a, mt * (2 * I / 256), st)));
+  const bool few_rows = (table ? o.rows_cap : int64_t(uni_m) * n_groups) < 64 * int64_t(n_groups);
+  MOE_TRY((launch_fp8<Epi::SWIGLU>(ta1, tb1, a, mt * (2 * I / 256), few_rows, st)));
   if (rec) MOE_TRY(rec->mark());
 
   GemmArgs b = a;
@@ -369,7 +379,7 @@ moe_status enqueue_ffn_fp8(const moe_dims& d, const FfnOperands& o, int n_groups
   b.a_scale_ld = o.rows_cap;
   b.b_scale = o.w2s;
   b.out_scale = nullptr;
-  MOE_TRY((launch_fp8<Epi::BF16>(ta2, tb2, b, mt * cdiv(D, 256), st)));
+  MOE_TRY((launch_fp8<Epi::BF16>(ta2, tb2, b, mt * cdiv(D, 256), few_rows, st)));
   return rec ? rec->mark() : MOE_OK;
 }
 
