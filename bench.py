@@ -418,7 +418,18 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=4, help="tokens per step of the reference arm")
     ap.add_argument("--profile-case", action="store_true",
                     help="only build the layer and run warmup+steps forwards (the command ncu wraps)")
+    ap.add_argument("--write-traffic", nargs=3, metavar=("KEY", "BYTES", "SOURCE"),
+                    help="record measured DRAM bytes per launch of KEY (workload/stage) in profiles/traffic.json, "
+                         "stamped with the hash of the current kernel sources; SOURCE says where the figure comes from")
     args = ap.parse_args()
+    if args.write_traffic:
+        key, nbytes, source = args.write_traffic
+        rec = json.load(open(PROFILE_TRAFFIC)) if os.path.exists(PROFILE_TRAFFIC) else {}
+        rec[key] = {"dram_bytes_per_launch": int(float(nbytes)), "sources_sha256": sources_hash(), "source": source}
+        with open(PROFILE_TRAFFIC, "w") as f:
+            json.dump(rec, f, indent=1, sort_keys=True)
+            f.write("\n")
+        return
     if args.profile_case:
         profile_case(args)
         return
