@@ -90,23 +90,26 @@ __device__ __forceinline__ bool f8decode(const GemmArgs& a, int tile, int items,
   return true;
 }
 
-// (a0, a1) += (v0, v1) * s as one packed fp32x2 FMA (each lane a correctly
-// rounded fp32 FMA, as fmaf).
-__device__ __forceinline__ void fma2(float& a0, float& a1, uint32_t v0, uint32_t v1, float s) {
-#if MOE_NO_F32X2
-  a0 = fmaf(__uint_as_float(v0), s, a0);
-  a1 = fmaf(__uint_as_float(v1), s, a1);
-#else
-  asm("{\n\t.reg .b64 acc, val, sc;\n\t"
-      "mov.b64 acc, {%0, %1};\n\t"
-      "mov.b64 val, {%2, %3};\n\t"
-      "mov.b64 sc, {%4, %4};\n\t"
-      "fma.rn.f32x2 acc, val, sc, acc;\n\t"
-      "mov.b64 {%0, %1}, acc;\n\t}"
-      : "+f"(a0), "+f"(a1)
-      : "r"(v0), "r"(v1), "f"(s));
-#endif
+// Promotion arithmetic on packed pairs: an accumulator pair is one 64-bit
+// register (two fp32 lanes), so fma.rn.f32x2 -- two correctly rounded fp32
+// FMAs, as fmaf -- needs no repacking of the accumulators.
+__device__ __forceinline__ uint64_t pair_of(float s) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(s));
+  return r;
 }
+
+// a += (v0, v1) * s2
+__device__ __forceinline__ void fma2(uint64_t& a, uint32_t v0, uint32_t v1, uint64_t s2) {
+  asm("{\n\t.reg .b64 val;\n\t"
+      "mov.b64 val, {%1, %2};\n\t"
+      "fma.rn.f32x2 %0, val, %3, %0;\n\t}"
+      : "+l"(a)
+      : "r"(v0), "r"(v1), "l"(s2));
+}
+
+__device__ __forceinline__ float lo_of(uint64_t a) { return __uint_as_float(static_cast<uint32_t>(a)); }
+__device__ __forceinline__ float hi_of(uint64_t a) { return __uint_as_float(static_cast<uint32_t>(a >> 32)); }
 
 template <Epi EPI, int EW>
 __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
@@ -283,9 +286,9 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
       const float* sb1_ptr = sb_ptr + (EPI == Epi::SWIGLU ? KB : (int64_t)blk * KB);  // up / my block
       float sa_next = a_in ? __ldg(sa_ptr) : 0.0f;
       float sb0_next = blk_ok ? __ldg(sb0_ptr) : 0.0f, sb1_next = blk_ok ? __ldg(sb1_ptr) : 0.0f;
-      float acc[NCH * 16];
+      uint64_t acc2[NCH * 8];  // acc2[c] = columns (2c, 2c + 1) of my NCH * 16
 #pragma unroll
-      for (int i = 0; i < NCH * 16; ++i) acc[i] = 0.0f;
+      for (int i = 0; i < NCH * 8; ++i) acc2[i] = 0;
 #pragma unroll 1
       for (int kb = 0; kb < num_kb; ++kb, ++it) {
         const uint32_t b = it & 1, u = it >> 1;
@@ -300,6 +303,7 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
         tc_fence_after();
         const uint32_t tb = t_lane + b * BN;
         if (warp_rows) {
+          const uint64_t s0p = pair_of(s0), s1p = pair_of(s1);
           if constexpr (CG == 2) {
             // the load of chunk j + 1 is in flight while the FMAs of chunk j run
             uint32_t va[16], vb[16];
@@ -310,9 +314,9 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
               uint32_t(&cur)[16] = (j & 1) ? vb : va;
               uint32_t(&nxt)[16] = (j & 1) ? va : vb;
               if (j + 1 < NCH) tmem_ld16_nowait(tb + col_of(j + 1), nxt);
-              const float sc = (EPI == Epi::SWIGLU && j >= NP) ? s1 : s0;
+              const uint64_t sc = (EPI == Epi::SWIGLU && j >= NP) ? s1p : s0p;
 #pragma unroll
-              for (int i = 0; i < 16; i += 2) fma2(acc[j * 16 + i], acc[j * 16 + i + 1], cur[i], cur[i + 1], sc);
+              for (int i = 0; i < 8; ++i) fma2(acc2[j * 8 + i], cur[2 * i], cur[2 * i + 1], sc);
               if (j + 1 < NCH) tmem_ld_wait(nxt);
             }
           } else {
@@ -323,9 +327,9 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
               uint32_t cur[16];
               tmem_ld16_nowait(tb + col_of(j), cur);
               tmem_ld_wait(cur);
-              const float sc = (EPI == Epi::SWIGLU && j >= NP) ? s1 : s0;
+              const uint64_t sc = (EPI == Epi::SWIGLU && j >= NP) ? s1p : s0p;
 #pragma unroll
-              for (int i = 0; i < 16; i += 2) fma2(acc[j * 16 + i], acc[j * 16 + i + 1], cur[i], cur[i + 1], sc);
+              for (int i = 0; i < 8; ++i) fma2(acc2[j * 8 + i], cur[2 * i], cur[2 * i + 1], sc);
             }
           }
         }
@@ -334,6 +338,12 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
         if (lane == 0) mbar_arrive(&acc_empty[b]);
       }
       if (!ok) break;
+      float acc[NCH * 16];
+#pragma unroll
+      for (int i = 0; i < NCH * 8; ++i) {
+        acc[2 * i] = lo_of(acc2[i]);
+        acc[2 * i + 1] = hi_of(acc2[i]);
+      }
       if constexpr (EPI == Epi::SWIGLU) {
         // h = SiLU(gate) * up for my NP * 16 features; the row's 1 x 128 scale
         // needs the amax of the other CG - 1 warps of the quarter too.
