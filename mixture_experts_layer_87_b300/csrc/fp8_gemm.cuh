@@ -15,10 +15,11 @@
 // issues TMA loads into a 4-stage ring (16 KB of tokens + 32 KB of weights
 // per 128-K stage), one thread of warp 1 issues kind::f8f6f4 MMAs (K = 32)
 // into one of two TMEM partial buffers (2 x 256 columns), the epilogue warps
-// promote: each reads 16-column slices of its lane quarter's share of the
-// partial, multiplies by s_x * s_w and adds into fp32 registers (packed
-// fp32x2 FMAs), then frees the buffer for the MMA two K blocks ahead.  Warps whose 32 rows all lie past
-// the group's end keep the barrier phases in step without loading anything.
+// promote: each reads its lane quarter's share of the partial in 16-column
+// slices, multiplies by s_x * s_w and adds into fp32 registers (packed fp32x2
+// FMAs), and frees the buffer for the MMA two K blocks ahead as soon as its
+// last slice is in registers.  Warps whose 32 rows all lie past the group's
+// end keep the barrier phases in step without loading anything.
 //
 // Epilogues:
 //   SWIGLU  the weight block holds 128 gate rows then the 128 matching up
@@ -38,7 +39,7 @@
 namespace moe {
 
 // EW epilogue warps, EW / 4 per TMEM lane quarter.  8: 128 accumulators per
-// thread and a software-pipelined TMEM read; 16: 64 accumulators per thread,
+// thread, TMEM read two slices per wait; 16: 64 accumulators per thread,
 // twice the warps on a quarter -- the better choice when few rows per tile
 // are valid (a decode step: 8 tokens per expert on average) and all the
 // work falls on one quarter.
@@ -302,22 +303,32 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t tb = t_lane + b * BN;
+        bool released = false;
         if (warp_rows) {
           const uint64_t s0p = pair_of(s0), s1p = pair_of(s1);
           if constexpr (CG == 2) {
-            // the load of chunk j + 1 is in flight while the FMAs of chunk j run
-            uint32_t va[16], vb[16];
-            tmem_ld16_nowait(tb + col_of(0), va);
-            tmem_ld_wait(va);
+            // pairs of 16-column loads, one wait per pair; the partial buffer is
+            // released as soon as the last pair has landed in registers, before
+            // its FMAs
 #pragma unroll
-            for (int j = 0; j < NCH; ++j) {
-              uint32_t(&cur)[16] = (j & 1) ? vb : va;
-              uint32_t(&nxt)[16] = (j & 1) ? va : vb;
-              if (j + 1 < NCH) tmem_ld16_nowait(tb + col_of(j + 1), nxt);
-              const uint64_t sc = (EPI == Epi::SWIGLU && j >= NP) ? s1p : s0p;
+            for (int j = 0; j < NCH; j += 2) {
+              uint32_t c0[16], c1[16];
+              tmem_ld16_nowait(tb + col_of(j), c0);
+              tmem_ld16_nowait(tb + col_of(j + 1), c1);
+              tmem_ld_wait(c0);
+              tmem_ld_wait(c1);
+              if (j + 2 == NCH) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[b]);
+                released = true;
+              }
+              const uint64_t sc0 = (EPI == Epi::SWIGLU && j >= NP) ? s1p : s0p;
+              const uint64_t sc1 = (EPI == Epi::SWIGLU && j + 1 >= NP) ? s1p : s0p;
 #pragma unroll
-              for (int i = 0; i < 8; ++i) fma2(acc2[j * 8 + i], cur[2 * i], cur[2 * i + 1], sc);
-              if (j + 1 < NCH) tmem_ld_wait(nxt);
+              for (int i = 0; i < 8; ++i) fma2(acc2[j * 8 + i], c0[2 * i], c0[2 * i + 1], sc0);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) fma2(acc2[(j + 1) * 8 + i], c1[2 * i], c1[2 * i + 1], sc1);
             }
           } else {
             // registers allow one chunk at a time; the other warps of the
@@ -333,9 +344,11 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
             }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[b]);
+        if (!released) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[b]);
+        }
       }
       if (!ok) break;
       float acc[NCH * 16];
