@@ -138,6 +138,10 @@ CONFIGS = {
                             rho=V3_RHO, alpha=V3_ALPHA),
     "v3_slice_fp8": LayerConfig("v3_slice_fp8", T=1024, d=7168, E=32, k=8, n_shared=1, inter=2048,
                                 prec="fp8", rho=V3_RHO, alpha=V3_ALPHA),
+    # Decode-shaped slice: 8 tokens per expert on average (as a V3 decode step
+    # of 256 tokens over 256 experts) with 32 experts, for profiling.
+    "decode_slice": LayerConfig("decode_slice", T=32, d=7168, E=32, k=8, n_shared=1, inter=2048,
+                                prec="fp8", bias="zero", rho=V3_RHO, alpha=DECODE_ALPHA),
     # Small parity shapes: several M/N/K tiles, ragged tails, odd expert counts.
     "ragged": LayerConfig("ragged", T=300, d=384, E=20, k=3, n_shared=1, inter=256,
                           rho=0.3, alpha=1.0),
