@@ -57,18 +57,13 @@ def dist_init():
 
 
 def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+    from mixture_experts_layer_87_b300 import replicas
+    replicas.barrier()
 
 
 def max_over_ranks(x: float, world: int) -> float:
-    if world == 1:
-        return x
-    import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    from mixture_experts_layer_87_b300 import replicas
+    return replicas.max_over_ranks(x, device="cuda")
 
 
 # ----------------------------------------------------------------------------
@@ -339,7 +334,9 @@ def run_reference(args, world, rank):
 
 def measure(cfg, args, world, pk, variants_only=False):
     layer = build_layer(cfg)
-    u_host = synth.tokens(cfg, step=0)
+    # every replica runs the layer on its own batch of T tokens (weak scaling)
+    rank = int(os.environ.get("RANK", "0"))
+    u_host = synth.tokens(cfg, step=rank)
     u = u_host.cuda()
     bias = synth.bias(cfg).cuda()
     out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
@@ -368,7 +365,11 @@ def measure_decode(args, world, pk, layer=None):
     cfg = synth.get_config("decode")
     if layer is None:
         layer = build_layer(cfg)
-    us = [synth.tokens(cfg, step=s).cuda() for s in range(cfg.steps)]
+    # replica r draws its tokens of step s from the stream position r * steps + s;
+    # the bias update sees the loads of all replicas (one all-reduce of E int32)
+    from mixture_experts_layer_87_b300 import replicas
+    rank = int(os.environ.get("RANK", "0"))
+    us = [synth.tokens(cfg, step=rank * cfg.steps + s).cuda() for s in range(cfg.steps)]
     bias = torch.zeros(cfg.E, dtype=torch.float32, device="cuda")
     out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
     counts = torch.zeros((cfg.steps, cfg.E), dtype=torch.int32, device="cuda")
@@ -376,7 +377,8 @@ def measure_decode(args, world, pk, layer=None):
     def loop(b):
         for s in range(cfg.steps):
             layer.forward(us[s], b, out, counts=counts[s])
-            capi.moe_bias_update(cfg.E, cfg.T, cfg.k, counts[s], cfg.gamma, b)
+            replicas.global_counts(counts[s])
+            capi.moe_bias_update(cfg.E, world * cfg.T, cfg.k, counts[s], cfg.gamma, b)
 
     loop(torch.zeros_like(bias))           # warm-up pass
     torch.cuda.synchronize()
@@ -385,7 +387,8 @@ def measure_decode(args, world, pk, layer=None):
     ev[0].record()
     for s in range(cfg.steps):
         layer.forward(us[s], bias, out, counts=counts[s])
-        capi.moe_bias_update(cfg.E, cfg.T, cfg.k, counts[s], cfg.gamma, bias)
+        replicas.global_counts(counts[s])
+        capi.moe_bias_update(cfg.E, world * cfg.T, cfg.k, counts[s], cfg.gamma, bias)
         ev[s + 1].record()
     torch.cuda.synchronize()
     barrier(world)
@@ -393,7 +396,7 @@ def measure_decode(args, world, pk, layer=None):
     total = max_over_ranks(sum(step_ms), world)
     stage_ms = time_stages(layer, us[0], bias, out, 5)
     c = counts.cpu().numpy()
-    mean = cfg.T * cfg.k / cfg.E
+    mean = world * cfg.T * cfg.k / cfg.E
     gbs = [layer_work(cfg, c[s])[1] / (step_ms[s] * 1e-3) / 1e9 for s in range(cfg.steps)]
     return {"value": world * cfg.T * cfg.steps / (total * 1e-3), "ms_per_step": total / cfg.steps,
             "hbm_gbs_mean": round(float(np.mean(gbs)), 1),
