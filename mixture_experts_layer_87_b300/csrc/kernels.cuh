@@ -256,11 +256,15 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
   if constexpr (!FP8) {
     uint4* dst = reinterpret_cast<uint4*>(x_perm);
     const int nc = d / 8;
-    for (int c = lane; c < nc; c += 32) {
-      const uint4 v = src[c];
+    // every lane runs every iteration (the shuffles need the whole warp);
+    // lanes past the row's last 16-byte chunk only skip the copy
+    for (int c0 = 0; c0 < nc; c0 += 32) {
+      const int c = c0 + lane;
+      const bool act = c < nc;
+      const uint4 v = act ? src[c] : make_uint4(0, 0, 0, 0);
       for (int j = 0; j < k; ++j) {
         const int s = __shfl_sync(0xffffffffu, my_slot, j);
-        if (s >= 0) dst[(int64_t)s * nc + c] = v;
+        if (act && s >= 0) dst[(int64_t)s * nc + c] = v;
       }
     }
   } else {

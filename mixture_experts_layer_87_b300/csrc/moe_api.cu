@@ -105,6 +105,7 @@ P* at(void* ws, size_t off) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool d_T_nonzero(const moe_dims* d) { return d->T != 0; }
 
 moe_status check_dims(const moe_dims* d) {
   if (!d) return MOE_ERR_INVALID_ARG;
@@ -243,6 +244,7 @@ moe_status enqueue_dispatch(const moe_dims& d, const int32_t* idx, const uint16_
                                   static_cast<int>(cgroup_cap(d)), status);
   MOE_TRY(launched());
   if (rec) MOE_TRY(rec->mark());
+  if (d.T == 0) return rec ? rec->mark() : MOE_OK;  // the offsets (all zero) are the whole result
   const unsigned blocks = static_cast<unsigned>(cdiv(int64_t(d.T) * 32, 256));
   const int64_t rows = int64_t(d.T) * d.k;
   const __nv_bfloat16* ub = reinterpret_cast<const __nv_bfloat16*>(u);
@@ -472,7 +474,9 @@ moe_status moe_route(const moe_dims* dims, const uint16_t* u, const uint16_t* ce
                      int32_t* topk_idx, float* topk_gate, int32_t* counts, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(check_dims(dims));
   MOE_TRY(check_ws(dims, ws, ws_bytes));
-  if (!u || !centroids || !bias || !topk_idx || !topk_gate || !counts) return MOE_ERR_INVALID_ARG;
+  // token-sized buffers may be empty (null) when T == 0
+  const bool empty = dims->T == 0;
+  if (!centroids || !bias || !counts || (!empty && (!u || !topk_idx || !topk_gate))) return MOE_ERR_INVALID_ARG;
   if (!aligned16(u) || !aligned16(centroids)) return MOE_ERR_INVALID_ARG;
   const Layout L = make_layout(*dims);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -487,8 +491,10 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, const uint
                        void* stream) {
   MOE_TRY(check_dims(dims));
   MOE_TRY(check_ws(dims, ws, ws_bytes));
-  if (!topk_idx || !u || !offsets || !perm || !slot || !x_perm) return MOE_ERR_INVALID_ARG;
-  if (dims->prec == MOE_FP8_E4M3 && !x_scale) return MOE_ERR_INVALID_ARG;
+  // token-sized buffers may be empty (null) when T == 0
+  const bool empty = dims->T == 0;
+  if (!offsets || (!empty && (!topk_idx || !u || !perm || !slot || !x_perm))) return MOE_ERR_INVALID_ARG;
+  if (dims->prec == MOE_FP8_E4M3 && !empty && !x_scale) return MOE_ERR_INVALID_ARG;
   if (!aligned16(u) || !aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
   const Layout L = make_layout(*dims);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -541,10 +547,10 @@ moe_status moe_grouped_ffn(const moe_dims* dims, int32_t n_groups, int32_t rows,
 moe_status moe_combine(const moe_dims* dims, const uint16_t* u, const uint16_t* shared_y, const uint16_t* y_perm,
                        const int32_t* slot, const float* topk_gate, uint16_t* out, void* stream) {
   MOE_TRY(check_dims(dims));
+  if (dims->T == 0) return MOE_OK;  // nothing to combine; the buffers may be empty (null)
   if (!u || !y_perm || !slot || !topk_gate || !out || (dims->n_shared > 0 && !shared_y)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(u) || !aligned16(y_perm) || !aligned16(out) || (shared_y && !aligned16(shared_y)))
     return MOE_ERR_INVALID_ARG;
-  if (dims->T == 0) return MOE_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   combine_kernel<<<dims->T, 128, 0, st>>>(
       reinterpret_cast<const __nv_bfloat16*>(u), reinterpret_cast<const __nv_bfloat16*>(shared_y), dims->n_shared,
@@ -572,7 +578,8 @@ moe_status moe_forward_profiled(const moe_dims* dims, const moe_weights* w, cons
   MOE_TRY(check_dims(dims));
   MOE_TRY(check_ws(dims, ws, ws_bytes));
   MOE_TRY(check_weights(*dims, w));
-  if (!u || !bias || !out || !aligned16(u) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  // u and out may be empty (null) when T == 0
+  if (!bias || (d_T_nonzero(dims) && (!u || !out)) || !aligned16(u) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
   if (events && n_events < MOE_PROFILE_EVENTS) return MOE_ERR_INVALID_ARG;
   const moe_dims& d = *dims;
   const bool fp8 = d.prec == MOE_FP8_E4M3;
@@ -714,7 +721,9 @@ extern "C" moe_status moe_route_noalloc(const moe_dims* dims, const uint16_t* u,
                                         const float* bias, int32_t* topk_idx, float* topk_gate, int32_t* counts,
                                         int32_t* device_status, void* stream) {
   MOE_TRY(check_dims(dims));
-  if (!u || !centroids || !bias || !topk_idx || !topk_gate || !counts) return MOE_ERR_INVALID_ARG;
+  // token-sized buffers may be empty (null) when T == 0
+  const bool empty = dims->T == 0;
+  if (!centroids || !bias || !counts || (!empty && (!u || !topk_idx || !topk_gate))) return MOE_ERR_INVALID_ARG;
   if (!aligned16(u) || !aligned16(centroids)) return MOE_ERR_INVALID_ARG;
   if (int64_t(dims->T) * dims->E > MOE_ROUTE_NOALLOC_MAX_LOGITS) return MOE_ERR_UNSUPPORTED;
   float* z = nullptr;

@@ -83,5 +83,18 @@ def rel_err(got: np.ndarray, ref: np.ndarray) -> float:
     return float(np.abs(got - ref).max() / np.sqrt((ref ** 2).mean()))
 
 
+def ffn_rel_err(got: np.ndarray, ref: np.ndarray, u: np.ndarray) -> float:
+    """max|err|/rms on the FFN part h' - u, with the unavoidable rounding of
+    the bf16 output taken out.  h' is stored as bf16 and dominated by u, so
+    half a bf16 ulp of h' can be a large share of the (much smaller) FFN part;
+    that rounding is the output format, not an error of the computation."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    mag = np.maximum(np.abs(ref), 2.0 ** -126)
+    half_ulp = np.exp2(np.floor(np.log2(mag)) - 8)       # bf16: 8 significant bits
+    excess = np.maximum(np.abs(got - ref) - half_ulp, 0.0)
+    return float(excess.max() / np.sqrt(np.mean((ref - np.asarray(u, np.float64)) ** 2)))
+
+
 def bf16_to_np(t: torch.Tensor) -> np.ndarray:
     return t.float().cpu().numpy().astype(np.float64)

@@ -8,7 +8,7 @@ import torch
 import oracle
 import synth
 from mixture_experts_layer_87_b300 import capi
-from parity import NEAR_TIE, TOL, HostLayer, bf16_to_np, check_selection, rel_err
+from parity import NEAR_TIE, TOL, HostLayer, bf16_to_np, check_selection, ffn_rel_err, rel_err
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -148,7 +148,7 @@ def _forward_parity(cfg, sample=None):
     got = bf16_to_np(out)[tokens]
     uref = oracle.bf16_to_f64(ub[tokens])
     err = rel_err(got, ref)
-    err_ffn = rel_err(got - uref, ref - uref)
+    err_ffn = ffn_rel_err(got, ref, uref)
     return err, err_ffn
 
 
