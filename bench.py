@@ -37,8 +37,10 @@ import synth  # noqa: E402
 METRIC = "MoE layer tokens/s at V3 shape (bf16, FP8); % of tensor/HBM roofline"
 UNIT = "tokens/s"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+# the sources of the expert GEMM kernels: a recorded DRAM-traffic figure is
+# reported only while these are unchanged since its ncu capture
 KERNEL_SOURCES = [os.path.join(ROOT, "mixture_experts_layer_87_b300", "csrc", f)
-                  for f in ("gemm.cuh", "expert_gemm.cuh", "fp8_gemm.cuh", "ptx.cuh", "kernels.cuh", "moe_api.cu")]
+                  for f in ("gemm.cuh", "expert_gemm.cuh", "fp8_gemm.cuh", "ptx.cuh")]
 
 
 # ----------------------------------------------------------------------------
