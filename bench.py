@@ -417,7 +417,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="v3", choices=["v3", "v3_fp8", "mid", "decode", "v3_slice", "v3_slice_fp8",
-                                                            "decode_slice"])
+                                                            "decode_slice", "v3_tokens", "v3_tokens_fp8"])
     ap.add_argument("--no-variants", action="store_true", help="skip the FP8 and decode measurements")
     ap.add_argument("--prec", default=None, choices=["bf16", "fp8"], help="override the workload's precision")
     ap.add_argument("--cpu-tokens", type=int, default=32, help="tokens in the CPU-oracle baseline sample")

@@ -138,6 +138,13 @@ CONFIGS = {
                             rho=V3_RHO, alpha=V3_ALPHA),
     "v3_slice_fp8": LayerConfig("v3_slice_fp8", T=1024, d=7168, E=32, k=8, n_shared=1, inter=2048,
                                 prec="fp8", rho=V3_RHO, alpha=V3_ALPHA),
+    # V3 token shapes (router, dispatch and combine are V3-sized: T, d, E and k
+    # are V3's) with tiny experts, so the whole layer fits a few GB: the
+    # workload ncu captures the bandwidth-bound kernels on.
+    "v3_tokens": LayerConfig("v3_tokens", T=8192, d=7168, E=256, k=8, n_shared=1, inter=128,
+                             rho=V3_RHO, alpha=V3_ALPHA),
+    "v3_tokens_fp8": LayerConfig("v3_tokens_fp8", T=8192, d=7168, E=256, k=8, n_shared=1, inter=128,
+                                 prec="fp8", rho=V3_RHO, alpha=V3_ALPHA),
     # Decode-shaped slice: 8 tokens per expert on average (as a V3 decode step
     # of 256 tokens over 256 experts) with 32 experts, for profiling.
     "decode_slice": LayerConfig("decode_slice", T=32, d=7168, E=32, k=8, n_shared=1, inter=2048,
