@@ -10,16 +10,27 @@
 // the promotion of a 128-K partial into fp32 costs one FMA per element.
 //
 // Work item = (group g, 256-column weight block n, 128-row tile m), m
-// fastest; one CTA per SM takes items from a shared queue (warp 10 fetches
+// fastest; one CTA per SM takes items from a shared queue (warp 2 fetches
 // and decodes them, see the item ring of expert_gemm.cuh).  Warp 0
 // issues TMA loads into a 4-stage ring (16 KB of tokens + 32 KB of weights
 // per 128-K stage), one thread of warp 1 issues kind::f8f6f4 MMAs (K = 32)
-// into one of two TMEM partial buffers (2 x 256 columns), the epilogue warps
-// promote: each reads its lane quarter's share of the partial in 16-column
-// slices, multiplies by s_x * s_w and adds into fp32 registers (packed fp32x2
-// FMAs), and frees the buffer for the MMA two K blocks ahead as soon as its
-// last slice is in registers.  Warps whose 32 rows all lie past the group's
-// end keep the barrier phases in step without loading anything.
+// into one of two TMEM partial buffers (2 x 256 columns), and the epilogue
+// warps (warps 4 .., two or four warpgroups) promote: each reads its lane
+// quarter's share of the partial in 16-column slices, multiplies by
+// s_x * s_w and adds into fp32 registers (packed fp32x2 FMAs), and frees the
+// buffer for the MMA two K blocks ahead as soon as its last slice is in
+// registers.  Warp 3 only lends its registers: the first warpgroup gives up
+// most of its registers to the epilogue warpgroups (setmaxnreg), so that an
+// epilogue warp can hold its 128 accumulators and four slices (64 more
+// registers) at once and wait for TMEM twice per K block instead of four
+// times.  Warps whose 32 rows all lie past the group's end keep the barrier
+// phases in step without loading anything.
+//
+// Between items the MMA can run only two K blocks ahead of the epilogue, so
+// the item tail is kept short: the scheduler warp stages the scales of an
+// item's first K blocks in its ring slot (their memory latency is spent up to
+// four items early), and the bf16 output rows leave through shared memory in
+// coalesced stores.
 //
 // Epilogues:
 //   SWIGLU  the weight block holds 128 gate rows then the 128 matching up
@@ -39,10 +50,15 @@
 namespace moe {
 
 // EW epilogue warps, EW / 4 per TMEM lane quarter.  8: 128 accumulators per
-// thread, TMEM read two slices per wait; 16: 64 accumulators per thread,
-// twice the warps on a quarter -- the better choice when few rows per tile
-// are valid (a decode step: 8 tokens per expert on average) and all the
-// work falls on one quarter.
+// thread, TMEM read four slices per wait; 16: 64 accumulators per thread,
+// one slice per wait, twice the warps on a quarter -- the better choice when
+// few rows per tile are valid (a decode step: 8 tokens per expert on
+// average) and all the work falls on one quarter.
+//
+// Registers: the block launches with LAUNCH_REGS per thread (the most that
+// __launch_bounds__(THREADS, 1) allows, which the host checks against the
+// compiled kernel); warpgroup 0 (producer, MMA, scheduler, lender) drops to
+// CTRL_REGS and the epilogue warpgroups rise to EPI_REGS.
 template <int EW>
 struct F8Shape {
   static constexpr int BM = 128, BN = 256, BK = 128, UK = 32;
@@ -50,15 +66,63 @@ struct F8Shape {
   static constexpr int STAGES = 4;
   static constexpr int EPI_WARPS = EW;
   static constexpr int CG = EW / 4;
-  static constexpr int THREADS = 32 * (3 + EW);  // producer, MMA, epilogue, scheduler
+  static constexpr int BATCH = CG == 2 ? 4 : 1;        // 16-column slices per TMEM wait
+  static constexpr int THREADS = 32 * (4 + EW);        // producer, MMA, scheduler, lender, epilogue
+  static constexpr int LAUNCH_REGS = 65536 / THREADS / 8 * 8;
+  static constexpr int CTRL_REGS = 48;
+  static constexpr int EPI_REGS = (LAUNCH_REGS * THREADS - 128 * CTRL_REGS) / (32 * EW) / 8 * 8;
   static_assert(CG == 2 || CG == 4, "column groups");
+  static_assert(128 * CTRL_REGS + 32 * EW * EPI_REGS <= LAUNCH_REGS * THREADS, "register split");
+  static_assert(EPI_REGS <= 256 && EPI_REGS >= LAUNCH_REGS, "register split");
+  // promotion scales of the first AHEAD K blocks of an item, staged in its
+  // ring slot by the scheduler warp: s_x of the 128 rows, then s_w of the
+  // two 128-column weight blocks, per K block; later K blocks are loaded
+  // AHEAD blocks before their use
+  static constexpr int AHEAD = 3;
+  static constexpr int SLOT_FLOATS = AHEAD * 128 + AHEAD * 2 + 2;
+  // bf16 results of 8 epilogue warps (256 bytes per row and warp) leave
+  // through a per-warp shared buffer, see warp_rows_out; the 64 code bytes
+  // per row of the SwiGLU epilogue, and the 16-warp shapes, store directly
+  template <Epi EPI>
+  __host__ __device__ static constexpr bool stage_out() {
+    return CG == 2 && EPI == Epi::BF16;
+  }
 };
 
-template <int EW>
+// Row-per-lane results to global rows.  Lane l holds 64 contiguous bytes of
+// row row0 + l; stored straight from the registers, each 16-byte store of the
+// warp would touch 32 rows (32 cache lines).  The warp writes its 32 x 64
+// bytes to a shared buffer instead (an 80-byte pitch puts the 16-byte writes
+// of 8 consecutive lanes in distinct banks) and stores them back with 4 lanes
+// per row: 8 rows, 8 lines, per instruction.  Rows at or past `rows` are not
+// written; every lane of the warp calls this.
+constexpr int kOutPitch = 80;
+constexpr int kOutWarpBytes = 32 * kOutPitch;
+
+__device__ __forceinline__ void warp_rows_out(uint8_t* wbuf, const uint4 (&v)[4], uint8_t* col0, int64_t ld_bytes,
+                                              int row0, int rows, int lane) {
+  uint4* mine = reinterpret_cast<uint4*>(wbuf + lane * kOutPitch);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) mine[q] = v[q];
+  __syncwarp();
+  const int part = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int row = i * 8 + (lane >> 2);
+    if (row < rows)
+      *reinterpret_cast<uint4*>(col0 + (int64_t)(row0 + row) * ld_bytes + part * 16) =
+          *reinterpret_cast<const uint4*>(wbuf + row * kOutPitch + part * 16);
+  }
+  __syncwarp();
+}
+
+template <Epi EPI, int EW>
 constexpr size_t fp8_gemm_smem_bytes() {
   using S = F8Shape<EW>;
   return 1024 + size_t(S::STAGES) * (S::A_BYTES + S::B_BYTES) + 512 /* barriers, item ring */ +
-         2 * S::CG * 128 * sizeof(float) /* amax exchange: 2 items x CG column groups x 128 rows */;
+         2 * S::CG * 128 * sizeof(float) /* amax exchange: 2 items x CG column groups x 128 rows */ +
+         kQueueSlots * S::SLOT_FLOATS * sizeof(float) /* staged scales */ +
+         (S::template stage_out<EPI>() ? size_t(EW) * kOutWarpBytes : 0) /* output staging */;
 }
 
 // Item -> (group, column block, row tile); the same ordering and table as
@@ -139,6 +203,9 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   ring.slot = reinterpret_cast<int*>(tmem_slot + 4);
   float* amax_x = reinterpret_cast<float*>(smem + STAGES * (A_BYTES + B_BYTES) + 512);  // [2][CG][128]
+  float* slot_scales = amax_x + 2 * S::CG * 128;  // [kQueueSlots][SLOT_FLOATS]
+  uint8_t* out_stage = reinterpret_cast<uint8_t*>(slot_scales + kQueueSlots * S::SLOT_FLOATS);  // [EW][32 x 80]
+  constexpr int AHEAD = S::AHEAD, SLOT_FLOATS = S::SLOT_FLOATS;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nb = (args.N + BN - 1) / BN;
@@ -170,89 +237,132 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 2 + S::EPI_WARPS) {
-    // ------------------------------------------------------------ item scheduler
-    if (lane == 0) {
+  if (warp < 4) {
+    // warpgroup 0: warp 3 only lends its registers to the epilogue warps
+    regs_release<S::CTRL_REGS>();
+    if (warp == 2) {
+      // ------------------------------------------------------------ item scheduler
+      // Lane 0 takes the items; the whole warp stages each item's first
+      // scales in its slot before publishing it, so their memory latency is
+      // spent up to kQueueSlots items ahead of the epilogue.
       const int items = args.groups == nullptr ? (args.uni_m + 127) / 128 * nb * args.n_groups
                                                : __ldg(args.mt_total) * nb;
+      const int KB = args.K / S::BK;
       int item = blockIdx.x;
       for (uint32_t lt = 0;; ++lt) {
         TileCoord tc{-1, 0, 0, 0, 0, 0};
-        const bool have = f8decode(args, item, items, nb, tc);
-        if (have) item = gridDim.x + atomicAdd(args.queue, 1);  // the next one, while this one is published
-        const int v[6] = {have ? tc.g : -1, tc.m_idx, tc.n_idx, tc.a_row, tc.out_row, tc.rows_valid};
-        if (!ring_put(ring, lt, v, args.status, abort_flag) || !have) break;
+        const bool have = f8decode(args, item, items, nb, tc);  // item is warp-uniform
+        if (have) {
+          int next = 0;
+          if (lane == 0) next = atomicAdd(args.queue, 1);  // the next one, while this one is staged
+          item = gridDim.x + __shfl_sync(0xffffffffu, next, 0);
+        }
+        const uint32_t s = lt % kQueueSlots;
+        if (lt >= kQueueSlots &&
+            !__all_sync(0xffffffffu, xwait(&ring.q_empty[s], ((lt / kQueueSlots) & 1) ^ 1, args.status, abort_flag)))
+          break;
+        if (have) {
+          float* ss = slot_scales + s * SLOT_FLOATS;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int row = tc.a_row + lane + 32 * i;
+            const bool in = row < args.a_rows_cap;
+#pragma unroll
+            for (int kb = 0; kb < AHEAD; ++kb)
+              ss[kb * 128 + lane + 32 * i] =
+                  kb < num_kb && in ? __ldg(args.a_scale + (int64_t)kb * args.a_scale_ld + row) : 0.0f;
+          }
+          if (lane < 2 * AHEAD) {
+            const int j = lane & 1, kb = lane >> 1;
+            const int blk_row = (tc.g * args.b_rows_per_group + tc.n_idx * BN) / 128 + j;
+            const bool blk_in = EPI == Epi::SWIGLU || tc.n_idx * BN + j * 128 < args.N;
+            ss[AHEAD * 128 + kb * 2 + j] =
+                kb < num_kb && blk_in ? __ldg(args.b_scale + (int64_t)blk_row * KB + kb) : 0.0f;
+          }
+        }
+        __threadfence_block();
+        __syncwarp();
+        if (lane == 0) {
+          volatile int* dst = ring.slot + s * 8;
+          const int v[6] = {have ? tc.g : -1, tc.m_idx, tc.n_idx, tc.a_row, tc.out_row, tc.rows_valid};
+#pragma unroll
+          for (int i = 0; i < 6; ++i) dst[i] = v[i];
+          mbar_arrive(&ring.q_full[s]);  // release: coordinates and scales
+        }
+        __syncwarp();
+        if (!have) break;
       }
-    }
-  } else if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      uint32_t it = 0, issued = 0;
-      for (uint32_t lt = 0;; ++lt) {
-        int v[6];
-        if (!ring_take(ring, lt, v, args.status, abort_flag, false) || v[0] < 0) break;
-        const int b_row = v[0] * args.b_rows_per_group + v[2] * BN, a_row = v[3];
+    } else if (warp == 0) {
+      // ------------------------------------------------------------ TMA producer
+      if (lane == 0) {
+        uint32_t it = 0, issued = 0;
+        for (uint32_t lt = 0;; ++lt) {
+          int v[6];
+          if (!ring_take(ring, lt, v, args.status, abort_flag, false) || v[0] < 0) break;
+          const int b_row = v[0] * args.b_rows_per_group + v[2] * BN, a_row = v[3];
+          bool ok = true;
+          for (int kb = 0; kb < num_kb; ++kb, ++it) {
+            const uint32_t s = it % STAGES;
+            if (it >= STAGES && !xwait(&empty[s], ((it / STAGES) & 1) ^ 1, args.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
+            tma_load_2d(sA + s * A_BYTES, &tmA, kb * S::BK, a_row, &full[s]);
+            tma_load_2d(sB + s * B_BYTES, &tmB, kb * S::BK, b_row, &full[s]);
+            issued = it + 1;
+          }
+          if (!ok) break;
+        }
+        // Abnormal exit only: copies still in flight land before the CTA leaves.
+        if (*abort_flag)
+          for (uint32_t j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
+            mbar_wait(&full[j % STAGES], (j / STAGES) & 1, args.status);
+      }
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        constexpr uint32_t idesc = idesc_make(0u, 128, BN);  // E4M3 x E4M3 -> fp32, M = 128, N = 256
+        uint32_t it = 0;
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb, ++it) {
-          const uint32_t s = it % STAGES;
-          if (it >= STAGES && !xwait(&empty[s], ((it / STAGES) & 1) ^ 1, args.status, abort_flag)) {
+        // the MMAs need no item coordinates (the producer placed the operands),
+        // only where the item stream ends
+        for (uint32_t lt = 0; ok; ++lt) {
+          int v[6];
+          if (!ring_take(ring, lt, v, args.status, abort_flag, false)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], A_BYTES + B_BYTES);
-          tma_load_2d(sA + s * A_BYTES, &tmA, kb * S::BK, a_row, &full[s]);
-          tma_load_2d(sB + s * B_BYTES, &tmB, kb * S::BK, b_row, &full[s]);
-          issued = it + 1;
+          if (v[0] < 0) break;
+          for (int kb = 0; kb < num_kb && ok; ++kb, ++it) {
+            const uint32_t s = it % STAGES, b = it & 1, u = it >> 1;
+            ok = xwait(&full[s], (it / STAGES) & 1, args.status, abort_flag);
+            if (ok && u > 0) ok = xwait(&acc_empty[b], (u & 1) ^ 1, args.status, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(sA + s * A_BYTES), b0 = smem_u32(sB + s * B_BYTES);
+  #pragma unroll
+            for (int k = 0; k < S::BK / S::UK; ++k)
+              mma_fp8(tmem_base + b * BN, sdesc_k128(a0 + k * 32), sdesc_k128(b0 + k * 32), idesc, k > 0 ? 1u : 0u);
+            mma_commit(&empty[s]);
+            mma_commit(&acc_full[b]);
+          }
         }
-        if (!ok) break;
+        if (!ok) *abort_flag = 1;
+        mma_commit(mma_done);  // every MMA of this CTA has completed before TMEM is released
+        mbar_wait(mma_done, 0, args.status);
       }
-      // Abnormal exit only: copies still in flight land before the CTA leaves.
-      if (*abort_flag)
-        for (uint32_t j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
-          mbar_wait(&full[j % STAGES], (j / STAGES) & 1, args.status);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_make(0u, 128, BN);  // E4M3 x E4M3 -> fp32, M = 128, N = 256
-      uint32_t it = 0;
-      bool ok = true;
-      // the MMAs need no item coordinates (the producer placed the operands),
-      // only where the item stream ends
-      for (uint32_t lt = 0; ok; ++lt) {
-        int v[6];
-        if (!ring_take(ring, lt, v, args.status, abort_flag, false)) {
-          ok = false;
-          break;
-        }
-        if (v[0] < 0) break;
-        for (int kb = 0; kb < num_kb && ok; ++kb, ++it) {
-          const uint32_t s = it % STAGES, b = it & 1, u = it >> 1;
-          ok = xwait(&full[s], (it / STAGES) & 1, args.status, abort_flag);
-          if (ok && u > 0) ok = xwait(&acc_empty[b], (u & 1) ^ 1, args.status, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + s * A_BYTES), b0 = smem_u32(sB + s * B_BYTES);
-#pragma unroll
-          for (int k = 0; k < S::BK / S::UK; ++k)
-            mma_fp8(tmem_base + b * BN, sdesc_k128(a0 + k * 32), sdesc_k128(b0 + k * 32), idesc, k > 0 ? 1u : 0u);
-          mma_commit(&empty[s]);
-          mma_commit(&acc_full[b]);
-        }
-      }
-      if (!ok) *abort_flag = 1;
-      mma_commit(mma_done);  // every MMA of this CTA has completed before TMEM is released
-      mbar_wait(mma_done, 0, args.status);
     }
   } else {
     // ------------------------------------------------------------ promotion + epilogue
+    regs_claim<S::EPI_REGS>();
     // The CG warps of one TMEM lane quarter split the 256 columns into CG
     // groups of NCH 16-column chunks.  SWIGLU: a warp takes NCH/2 gate
     // chunks of columns [0, 128) and the matching up chunks of [128, 256)
     // (gate feature f and up feature f stay in one thread); plain: NCH
     // consecutive chunks, all inside one 128-column weight block.
-    constexpr int CG = S::CG, NCH = 16 / CG, NP = NCH / 2;
-    const int ew = warp - 2;
+    constexpr int CG = S::CG, NCH = 16 / CG, NP = NCH / 2, BATCH = S::BATCH;
+    const int ew = warp - 4;
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int cg = ew >> 2;
     const int r = quarter * 32 + lane;
@@ -268,10 +378,26 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
     uint32_t it = 0, qphase = 0;
     bool ok = true;
     for (uint32_t lt = 0;; ++lt) {
+      // take item lt with its staged scales: (sa, sb0, sb1)[i] belong to the
+      // i-th K block from now
+      float sa[AHEAD], sb0[AHEAD], sb1[AHEAD];
       int v[6];
-      if (!ring_take(ring, lt, v, args.status, abort_flag, true)) {
-        ok = false;
-        break;
+      {
+        const uint32_t s = lt % kQueueSlots;
+        ok = __all_sync(0xffffffffu, xwait(&ring.q_full[s], (lt / kQueueSlots) & 1, args.status, abort_flag));
+        if (!ok) break;
+        const volatile int* src = ring.slot + s * 8;
+#pragma unroll
+        for (int i = 0; i < 6; ++i) v[i] = src[i];
+        const volatile float* ss = slot_scales + s * SLOT_FLOATS;
+#pragma unroll
+        for (int i = 0; i < AHEAD; ++i) {
+          sa[i] = ss[i * 128 + r];
+          sb0[i] = ss[AHEAD * 128 + i * 2 + (EPI == Epi::SWIGLU ? 0 : blk)];
+          sb1[i] = ss[AHEAD * 128 + i * 2 + (EPI == Epi::SWIGLU ? 1 : blk)];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ring.q_empty[s]);
       }
       if (v[0] < 0) break;
       const TileCoord tc{v[0], v[1], v[2], v[3], v[4], v[5]};
@@ -285,19 +411,23 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
       const bool blk_ok = EPI == Epi::SWIGLU || tc.n_idx * BN + blk * 128 < args.N;
       const float* sb0_ptr = sb_ptr + (int64_t)blk * KB;                          // gate / my block
       const float* sb1_ptr = sb_ptr + (EPI == Epi::SWIGLU ? KB : (int64_t)blk * KB);  // up / my block
-      float sa_next = a_in ? __ldg(sa_ptr) : 0.0f;
-      float sb0_next = blk_ok ? __ldg(sb0_ptr) : 0.0f, sb1_next = blk_ok ? __ldg(sb1_ptr) : 0.0f;
       uint64_t acc2[NCH * 8];  // acc2[c] = columns (2c, 2c + 1) of my NCH * 16
 #pragma unroll
       for (int i = 0; i < NCH * 8; ++i) acc2[i] = 0;
 #pragma unroll 1
       for (int kb = 0; kb < num_kb; ++kb, ++it) {
         const uint32_t b = it & 1, u = it >> 1;
-        const float s0 = sa_next * sb0_next, s1 = sa_next * sb1_next;
-        if (kb + 1 < num_kb) {  // scales one K block ahead
-          sa_next = a_in ? __ldg(sa_ptr + (int64_t)(kb + 1) * args.a_scale_ld) : 0.0f;
-          sb0_next = blk_ok ? __ldg(sb0_ptr + kb + 1) : 0.0f;
-          sb1_next = blk_ok ? __ldg(sb1_ptr + kb + 1) : 0.0f;
+        const float s0 = sa[0] * sb0[0], s1 = sa[0] * sb1[0];
+#pragma unroll
+        for (int i = 0; i + 1 < AHEAD; ++i) {
+          sa[i] = sa[i + 1];
+          sb0[i] = sb0[i + 1];
+          sb1[i] = sb1[i + 1];
+        }
+        if (kb + AHEAD < num_kb) {
+          sa[AHEAD - 1] = a_in ? __ldg(sa_ptr + (int64_t)(kb + AHEAD) * args.a_scale_ld) : 0.0f;
+          sb0[AHEAD - 1] = blk_ok ? __ldg(sb0_ptr + kb + AHEAD) : 0.0f;
+          sb1[AHEAD - 1] = blk_ok ? __ldg(sb1_ptr + kb + AHEAD) : 0.0f;
         }
         ok = __all_sync(0xffffffffu, xwait(&acc_full[b], u & 1, args.status, abort_flag));
         if (!ok) break;
@@ -306,41 +436,26 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
         bool released = false;
         if (warp_rows) {
           const uint64_t s0p = pair_of(s0), s1p = pair_of(s1);
-          if constexpr (CG == 2) {
-            // pairs of 16-column loads, one wait per pair; the partial buffer is
-            // released as soon as the last pair has landed in registers, before
-            // its FMAs
+          // BATCH 16-column slices per wait; the partial buffer is released
+          // as soon as the last batch has landed in registers, before its FMAs
 #pragma unroll
-            for (int j = 0; j < NCH; j += 2) {
-              uint32_t c0[16], c1[16];
-              tmem_ld16_nowait(tb + col_of(j), c0);
-              tmem_ld16_nowait(tb + col_of(j + 1), c1);
-              tmem_ld_wait(c0);
-              tmem_ld_wait(c1);
-              if (j + 2 == NCH) {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[b]);
-                released = true;
-              }
-              const uint64_t sc0 = (EPI == Epi::SWIGLU && j >= NP) ? s1p : s0p;
-              const uint64_t sc1 = (EPI == Epi::SWIGLU && j + 1 >= NP) ? s1p : s0p;
+          for (int j0 = 0; j0 < NCH; j0 += BATCH) {
+            uint32_t c[BATCH][16];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) fma2(acc2[j * 8 + i], c0[2 * i], c0[2 * i + 1], sc0);
+            for (int q = 0; q < BATCH; ++q) tmem_ld16_nowait(tb + col_of(j0 + q), c[q]);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) fma2(acc2[(j + 1) * 8 + i], c1[2 * i], c1[2 * i + 1], sc1);
+            for (int q = 0; q < BATCH; ++q) tmem_ld_wait(c[q]);
+            if (j0 + BATCH == NCH) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&acc_empty[b]);
+              released = true;
             }
-          } else {
-            // registers allow one chunk at a time; the other warps of the
-            // scheduler hide the load latency
 #pragma unroll
-            for (int j = 0; j < NCH; ++j) {
-              uint32_t cur[16];
-              tmem_ld16_nowait(tb + col_of(j), cur);
-              tmem_ld_wait(cur);
-              const uint64_t sc = (EPI == Epi::SWIGLU && j >= NP) ? s1p : s0p;
+            for (int q = 0; q < BATCH; ++q) {
+              const uint64_t sc = (EPI == Epi::SWIGLU && j0 + q >= NP) ? s1p : s0p;
 #pragma unroll
-              for (int i = 0; i < 8; ++i) fma2(acc2[j * 8 + i], cur[2 * i], cur[2 * i + 1], sc);
+              for (int i = 0; i < 8; ++i) fma2(acc2[(j0 + q) * 8 + i], c[q][2 * i], c[q][2 * i + 1], sc);
             }
           }
         }
@@ -393,6 +508,22 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
             reinterpret_cast<uint4*>(q)[w] = pk;
           }
           if (cg == 0) args.out_scale[(int64_t)tc.n_idx * args.out_scale_ld + tc.out_row + r] = scale;
+        }
+      } else if constexpr (S::template stage_out<EPI>()) {
+        if (warp_rows && blk_ok) {
+          uint8_t* ycol = static_cast<uint8_t*>(args.out) + (int64_t)(tc.n_idx * BN + cg * NCH * 16) * 2;
+#pragma unroll
+          for (int c = 0; c < NCH / 2; ++c) {
+            uint4 w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float* f = acc + c * 32 + q * 8;
+              w[q] = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                                pack_bf16x2(f[6], f[7]));
+            }
+            warp_rows_out(out_stage + ew * kOutWarpBytes, w, ycol + c * 64, (int64_t)args.out_ld * 2,
+                          tc.out_row + quarter * 32, tc.rows_valid - quarter * 32, lane);
+          }
         }
       } else {
         if (row_ok && blk_ok) {

@@ -291,8 +291,14 @@ moe_status launch_xgemm(const CUtensorMap& tw, const CUtensorMap& tx, const XGem
 template <Epi EPI, int EW>
 moe_status launch_fp8_ew(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int64_t grid,
                          cudaStream_t st) {
-  constexpr size_t smem = fp8_gemm_smem_bytes<EW>();
+  constexpr size_t smem = fp8_gemm_smem_bytes<EPI, EW>();
   auto kern = fp8_gemm_kernel<EPI, EW>;
+  // The kernel moves registers between its warpgroups (setmaxnreg); its split
+  // adds up to exactly LAUNCH_REGS per thread, so a build that launched with
+  // fewer would leave the epilogue warps waiting for registers forever.
+  cudaFuncAttributes fa;
+  MOE_TRY(cuda_ok(cudaFuncGetAttributes(&fa, kern)));
+  if (fa.numRegs != F8Shape<EW>::LAUNCH_REGS) return MOE_ERR_CUDA;
   MOE_TRY(cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))));
   kern<<<static_cast<unsigned>(grid), F8Shape<EW>::THREADS, smem, st>>>(ta, tb, a);
   return launched();

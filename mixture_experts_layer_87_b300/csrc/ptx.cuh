@@ -202,4 +202,19 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[16]) {
                : "memory");
 }
 
+// Per-warpgroup register budgets (setmaxnreg): every warp of a warpgroup
+// executes the same call.  The block's register file stays what it was
+// launched with, so the budgets of all warpgroups must add up to at most the
+// launch's registers per thread x threads, or an increase would never be
+// granted; the kernels that use these assert that sum at compile time and the
+// host checks the compiled register count before launching them.
+template <uint32_t R>
+__device__ __forceinline__ void regs_release() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <uint32_t R>
+__device__ __forceinline__ void regs_claim() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+
 }  // namespace moe
