@@ -52,7 +52,9 @@ typedef enum {
   MOE_ERR_INVALID_ARG = 1,  /* null pointer, bad shape, k > E, misaligned pointer */
   MOE_ERR_UNSUPPORTED = 2,  /* shape outside the limits above */
   MOE_ERR_WORKSPACE = 3,    /* workspace smaller than moe_workspace_size() */
-  MOE_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, attribute, ...) */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime call failed (launch, attribute, ...), or the FP8 GEMM
+                               was compiled to another register count than its warpgroup register
+                               split assumes (a build problem: nothing is launched) */
   MOE_ERR_TIMEOUT = 5,      /* device: a bounded wait inside a kernel ran out */
   MOE_ERR_BAD_INDEX = 6     /* device: an expert index outside [0, E) */
 } moe_status;
