@@ -70,13 +70,35 @@ def max_over_ranks(x: float, world: int) -> float:
 
 # ----------------------------------------------------------------------------
 # peaks and clocks
-def peaks():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(path):
+FALLBACK_PEAKS = dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0)
+
+
+def _peak_number(v):
+    """A peak given as a number, or as an object holding one (value / median / mean)."""
+    if isinstance(v, (int, float)) and not isinstance(v, bool):
+        return float(v)
+    if isinstance(v, str):
+        return float(v)
+    if isinstance(v, dict):
+        for key in ("value", "median", "mean", "gbs", "tflops"):
+            if key in v:
+                return _peak_number(v[key])
+    raise ValueError(f"no number in {v!r}")
+
+
+def peaks(path=None):
+    """Roofline denominators: the measured peaks when MEASURED_PEAKS.json
+    is present and readable, else the fallback figures (source says which)."""
+    path = path or os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if not os.path.exists(path):
+        return dict(FALLBACK_PEAKS, source="fallback")
+    try:
         p = json.load(open(path))
-        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"], bf16_sus=p.get("bf16_tflops_sustained", p["bf16_tflops"]),
-                    source="measured")
-    return dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0, source="fallback")
+        bf16 = _peak_number(p["bf16_tflops"])
+        sus = _peak_number(p["bf16_tflops_sustained"]) if "bf16_tflops_sustained" in p else bf16
+        return dict(hbm=_peak_number(p["hbm_gbs"]), bf16=bf16, bf16_sus=sus, source="measured")
+    except (OSError, ValueError, KeyError, TypeError) as e:
+        return dict(FALLBACK_PEAKS, source=f"fallback (MEASURED_PEAKS.json unreadable: {type(e).__name__})")
 
 
 class ClockSampler:
