@@ -88,7 +88,10 @@ def _peak_number(v):
 
 def peaks(path=None):
     """Roofline denominators: the measured peaks when MEASURED_PEAKS.json
-    is present and readable, else the fallback figures (source says which)."""
+    is present and readable, else the fallback figures (source says which).
+    bf16 is the burst figure (cuBLAS timed alone, at full clocks): the expert
+    GEMMs are timed one forward at a time, a few milliseconds each, not in a
+    seconds-long loop at the power cap.  bf16_sus is reported beside it."""
     path = path or os.path.join(ROOT, "MEASURED_PEAKS.json")
     if not os.path.exists(path):
         return dict(FALLBACK_PEAKS, source="fallback")
@@ -99,6 +102,43 @@ def peaks(path=None):
         return dict(hbm=_peak_number(p["hbm_gbs"]), bf16=bf16, bf16_sus=sus, source="measured")
     except (OSError, ValueError, KeyError, TypeError) as e:
         return dict(FALLBACK_PEAKS, source=f"fallback (MEASURED_PEAKS.json unreadable: {type(e).__name__})")
+
+
+def measure_fp8_peak():
+    """Dense FP8 (E4M3 x E4M3 -> bf16, fp32 accumulation) tensor throughput of
+    this GPU: cuBLASLt through torch._scaled_mm at 8192^3 (2 N^3 flops), best
+    of 10, CUDA events.  None if the call is not available here."""
+    try:
+        n = 8192
+        g = torch.Generator(device="cuda").manual_seed(0)
+        a = torch.randn((n, n), device="cuda", generator=g).to(torch.float8_e4m3fn)
+        b = torch.randn((n, n), device="cuda", generator=g).to(torch.float8_e4m3fn)
+        one = torch.ones((), device="cuda", dtype=torch.float32)
+        bt = b.t()                                  # column-major second operand
+        for _ in range(3):
+            torch._scaled_mm(a, bt, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        best = float("inf")
+        for _ in range(10):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            torch._scaled_mm(a, bt, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e.record()
+            torch.cuda.synchronize()
+            best = min(best, s.elapsed_time(e))
+        del a, b, bt
+        torch.cuda.empty_cache()
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except Exception:  # pragma: no cover - depends on the torch build
+        return None
+
+
+def tensor_peak(cfg, pk):
+    """(TFLOP/s, description) the expert GEMMs of this precision are measured against."""
+    if cfg.prec == "bf16":
+        return pk["bf16"], f"bf16 burst ({pk['source']})"
+    if pk.get("fp8"):
+        return pk["fp8"], "fp8 measured here: cuBLASLt E4M3 8192^3, best of 10"
+    return 2 * pk["bf16"], f"2 x bf16 burst ({pk['source']}; nominal fp8:bf16 ratio, fp8 not measurable here)"
 
 
 class ClockSampler:
@@ -116,22 +156,27 @@ class ClockSampler:
             self.uuid = None
 
     def start(self):
+        if not self.uuid:
+            return                      # without this GPU's id, other GPUs' clocks could be reported
+        gid = self.uuid if self.uuid.startswith("GPU-") else "GPU-" + self.uuid
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", gid, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
 
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            why = "nvidia-smi unavailable" if self.uuid else "GPU uuid unknown: not sampled"
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [why]}
         time.sleep(0.25)
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
         rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
-        if self.uuid:
-            mine = [r for r in rows if self.uuid.replace("GPU-", "") in r[0]]
-            rows = mine or rows
+        rows = [r for r in rows if self.uuid.replace("GPU-", "") in r[0]]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no sample of this GPU's uuid"], "samples": 0}
         sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
         smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -218,18 +263,24 @@ def sources_hash() -> str:
 
 
 def roofline(cfg, stage_ms: dict, counts, pk, kernel="routed_gate_up"):
+    """The kernel against its roofline: the slower of its algorithmic flops at
+    the tensor peak and its algorithmic bytes at the HBM copy bandwidth.
+    tensor_frac and hbm_frac give both sides; frac is the bound's."""
     F, B = stage_work(cfg, counts)[kernel]
     t = stage_ms[kernel] * 1e-3
-    tens_peak = (pk["bf16_sus"] if cfg.prec == "bf16" else 2 * pk["bf16_sus"]) * 1e12
-    t_f, t_b = F / tens_peak, B / (pk["hbm"] * 1e9)
+    peak_tf, peak_what = tensor_peak(cfg, pk)
+    t_f, t_b = F / (peak_tf * 1e12), B / (pk["hbm"] * 1e9)
     if t_f >= t_b:
-        ach, peak, unit, bound = F / t / 1e12, tens_peak / 1e12, "TFLOP/s", "tensor"
+        ach, peak, unit, bound = F / t / 1e12, peak_tf, "TFLOP/s", "tensor"
     else:
         ach, peak, unit, bound = B / t / 1e9, pk["hbm"], "GB/s", "hbm"
     return {"kernel": kernel, "bound": bound, "achieved": round(ach, 2), "peak": round(peak, 1), "unit": unit,
             "frac": round(ach / peak, 4), "traffic": kernel_traffic(kernel, cfg.name),
+            "tensor_frac": round(t_f / t, 4), "hbm_frac": round(t_b / t, 4),
+            "tflops": round(F / t / 1e12, 1), "gbs": round(B / t / 1e9, 1),
             "algorithmic_bytes": int(B), "algorithmic_flops": int(F), "ms": round(stage_ms[kernel], 4),
-            "peak_source": f"{pk['source']} ({'bf16 sustained' if cfg.prec == 'bf16' else '2 x bf16 sustained (nominal fp8:bf16 ratio)'}; HBM copy)"}
+            "peak_source": f"tensor: {peak_what}; HBM: copy bandwidth ({pk['source']})",
+            "frac_of_sustained_bf16": round(F / t / 1e12 / (pk["bf16_sus"] * (1 if cfg.prec == "bf16" else 2)), 4)}
 
 
 # ----------------------------------------------------------------------------
@@ -268,52 +319,52 @@ def time_stages(layer, u, bias, out, steps):
 
 
 def time_e2e(layer, u_host, bias, steps, warmup, world):
-    """Same metric through the public call with host buffers: H2D of u and
-    D2H of h' inside the timed region, every step."""
-    u_dev = torch.empty_like(u_host, device="cuda")
-    out_dev = torch.empty((layer.T, layer.d), dtype=torch.bfloat16, device="cuda")
-    out_host = torch.empty((layer.T, layer.d), dtype=torch.bfloat16, pin_memory=True)
-
-    def step():
-        u_dev.copy_(u_host, non_blocking=True)
-        layer.forward(u_dev, bias, out_dev)
-        out_host.copy_(out_dev, non_blocking=True)
-
-    for _ in range(warmup):
-        step()
+    """Same metric through the public call with host buffers: every step copies
+    its u from pinned host memory to the device and its h' back, inside the
+    timed region; the copies of neighbouring steps overlap the forward
+    (layer.HostPipeline)."""
+    from mixture_experts_layer_87_b300 import HostPipeline
+    pipe = HostPipeline(layer)
+    out_host = [torch.empty((layer.T, layer.d), dtype=torch.bfloat16, pin_memory=True)
+                for _ in range(HostPipeline.DEPTH)]
+    outs = lambda n: [out_host[i % len(out_host)] for i in range(n)]
+    pipe.run([u_host] * warmup, bias, outs(warmup))
     torch.cuda.synchronize()
     barrier(world)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record()
-    for _ in range(steps):
-        step()
+    pipe.run([u_host] * steps, bias, outs(steps))
     e.record()
     torch.cuda.synchronize()
     barrier(world)
     ms = s.elapsed_time(e) / steps
-    return ms, u_host.numel() * 2, out_host.numel() * 2
+    return ms, u_host.numel() * 2, out_host[0].numel() * 2
 
 
 # ----------------------------------------------------------------------------
 # CPU oracle (baseline leg and reference arm)
 def oracle_sample(cfg, u_host, sample, cache=None):
     """Time the oracle on tokens `sample` of the batch: routing + the full
-    layer output of those tokens.  Input generation is excluded."""
+    layer output of those tokens.  Input generation is excluded (timed and
+    subtracted); with a cache dict the generated expert weights are kept for
+    the next call."""
     import oracle
     ub = synth.bf16_bits(u_host)[sample]
     cent = synth.bf16_bits(synth.centroids(cfg))
     bias = np.asarray(synth.bias(cfg))
     gen = [0.0]
-    cache = {} if cache is None else cache
 
     def getter(shared):
         def f(e):
             key = (shared, e)
-            if key not in cache:
-                t0 = time.perf_counter()
-                cache[key] = tuple(synth.bf16_bits(w).copy() for w in synth.expert_weights(cfg, e, shared=shared))
-                gen[0] += time.perf_counter() - t0
-            return cache[key]
+            if cache is not None and key in cache:
+                return cache[key]
+            t0 = time.perf_counter()
+            w = tuple(synth.bf16_bits(w).copy() for w in synth.expert_weights(cfg, e, shared=shared))
+            gen[0] += time.perf_counter() - t0
+            if cache is not None:
+                cache[key] = w
+            return w
         return f
 
     t0 = time.perf_counter()
@@ -323,6 +374,16 @@ def oracle_sample(cfg, u_host, sample, cache=None):
     return time.perf_counter() - t0 - gen[0]
 
 
+def oracle_route_all(cfg, u_host):
+    """Seconds the oracle takes to route the whole batch."""
+    import oracle
+    ub = synth.bf16_bits(u_host)
+    cent = synth.bf16_bits(synth.centroids(cfg))
+    t0 = time.perf_counter()
+    oracle.route(ub, cent, np.asarray(synth.bias(cfg)), cfg.k)
+    return time.perf_counter() - t0
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -330,14 +391,41 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
+def host_cpu_model() -> str:
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def workload_config(cfg, world=1):
+    """The `config` object of the bench line; the reference arm prints the same."""
+    wbytes = (cfg.E + cfg.n_shared) * 3 * cfg.d * cfg.inter * (2 if cfg.prec == "bf16" else 1)
+    shape = "DeepSeek-V3-shaped" if cfg.d == 7168 else "mid-sized"
+    return {"workload": f"{shape} MoE layer forward ({cfg.name}): T={cfg.T}, d={cfg.d}, {cfg.E} routed experts "
+                        f"top-{cfg.k} + {cfg.n_shared} shared, I={cfg.inter}, {cfg.prec}, clustered tokens",
+            "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k, "n_shared": cfg.n_shared, "inter": cfg.inter,
+            "prec": cfg.prec, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": f"inputs larger than L2: every step streams the expert weights ({wbytes / 1e9:.1f} GB)"}
+
+
 # ----------------------------------------------------------------------------
 def run_reference(args, world, rank):
+    """The CPU oracle on this host's cores, on bounded samples of the workload:
+    each step takes the routing and the full layer output of a strided token
+    sample, sized so that all warm-up and timed steps take a few minutes."""
     if rank != 0:
         return
     cfg = synth.get_config(args.workload)
     u = synth.tokens(cfg)
-    per_step = max(1, args.ref_tokens)
-    sample = np.arange(0, cfg.T, cfg.T // per_step)[:per_step]
+    # ~0.25 s of oracle work per sampled token when the sample is small (few
+    # rows per expert to spread over the cores): ~150 s for the whole run
+    per_step = args.ref_tokens or int(min(512, max(4, 150.0 / (args.steps + args.warmup) / 0.25)))
+    stride = max(1, cfg.T // per_step)
+    sample = np.arange(0, cfg.T, stride)[:per_step]
     cache = {}
     for _ in range(args.warmup):
         oracle_sample(cfg, u, sample, cache)
@@ -347,16 +435,17 @@ def run_reference(args, world, rank):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k,
-                       "n_shared": cfg.n_shared, "inter": cfg.inter, "prec": cfg.prec},
+            "config": workload_config(cfg, args.gpus),
             "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-                             "sample": f"{per_step} tokens of the {cfg.T}-token batch per step (routing + full "
-                                       f"layer output), fp64 C oracle, input generation excluded"},
+                             "cpu": host_cpu_model(),
+                             "sample": f"{per_step} tokens (every {stride}th) of the {cfg.T}-token batch per step: "
+                                       f"routing + full layer output in the fp64 C oracle (OpenMP over rows), "
+                                       f"input generation excluded"},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def measure(cfg, args, world, pk, variants_only=False):
+def measure(cfg, args, world, pk):
     layer = build_layer(cfg)
     # every replica runs the layer on its own batch of T tokens (weak scaling)
     rank = int(os.environ.get("RANK", "0"))
@@ -373,14 +462,23 @@ def measure(cfg, args, world, pk, variants_only=False):
     ms = max_over_ranks(ms, world)
     stage_ms = time_stages(layer, u, bias, out, max(3, args.steps // 2))
     F, B = layer_work(cfg, counts_np)
-    tens_peak = (pk["bf16_sus"] if cfg.prec == "bf16" else 2 * pk["bf16_sus"]) * 1e12
-    t_roof = max(F / tens_peak, B / (pk["hbm"] * 1e9))
+    peak_tf, _ = tensor_peak(cfg, pk)
+    t_f, t_b = F / (peak_tf * 1e12), B / (pk["hbm"] * 1e9)
     res = {"ms_per_step": ms, "value": world * cfg.T / (ms * 1e-3), "stage_ms": stage_ms,
            "roofline": roofline(cfg, stage_ms, counts_np, pk),
-           "layer_roofline_frac": t_roof / (ms * 1e-3),
+           "layer_roofline_frac": max(t_f, t_b) / (ms * 1e-3),
+           "layer_bound": "tensor" if t_f >= t_b else "hbm",
+           "layer_tflops": F / (ms * 1e-3) / 1e12, "layer_gbs": B / (ms * 1e-3) / 1e9,
            "max_over_mean_load": float(counts_np.max() / (cfg.T * cfg.k / cfg.E)),
            "layer": layer, "u_host": u_host, "bias": bias, "counts": counts_np}
     return res
+
+
+def variant_summary(r):
+    return {"value": round(r["value"], 1), "ms_per_step": round(r["ms_per_step"], 4), "roofline": r["roofline"],
+            "layer_roofline_frac": round(r["layer_roofline_frac"], 4), "layer_bound": r["layer_bound"],
+            "layer_tflops": round(r["layer_tflops"], 1), "max_over_mean_load": round(r["max_over_mean_load"], 3),
+            "stage_ms": {k: round(v, 4) for k, v in r["stage_ms"].items()}}
 
 
 def measure_decode(args, world, pk, layer=None):
@@ -432,6 +530,22 @@ def measure_decode(args, world, pk, layer=None):
                          for m, g, x in zip(step_ms, gbs, c)]}
 
 
+def cpu_baseline_leg(cfg, u_host, n_sample):
+    """The oracle beside the GPU: routing of the whole batch, and the routing +
+    full layer output of a strided sample of n_sample tokens (tokens are
+    independent, so the sample's tokens/s is the layer's)."""
+    stride = max(1, cfg.T // n_sample)
+    sample = np.arange(0, cfg.T, stride)[:n_sample]
+    secs = oracle_sample(cfg, u_host, sample)
+    route_s = oracle_route_all(cfg, u_host)
+    return {"value": round(len(sample) / secs, 3), "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+            "cpu": host_cpu_model(), "seconds": round(secs, 2),
+            "route_all_tokens_per_s": round(cfg.T / route_s, 1),
+            "sample": f"{len(sample)} tokens (every {stride}th) of the {cfg.T}-token batch: routing + full layer "
+                      f"output in the fp64 C oracle (OpenMP over rows), input generation excluded; the routing "
+                      f"of all {cfg.T} tokens is timed apart (route_all_tokens_per_s)"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -440,10 +554,12 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="v3", choices=["v3", "v3_fp8", "mid", "decode", "v3_slice", "v3_slice_fp8",
                                                             "decode_slice", "v3_tokens", "v3_tokens_fp8"])
-    ap.add_argument("--no-variants", action="store_true", help="skip the FP8 and decode measurements")
+    ap.add_argument("--no-variants", action="store_true", help="skip the mid, FP8 and decode measurements")
     ap.add_argument("--prec", default=None, choices=["bf16", "fp8"], help="override the workload's precision")
-    ap.add_argument("--cpu-tokens", type=int, default=32, help="tokens in the CPU-oracle baseline sample")
-    ap.add_argument("--ref-tokens", type=int, default=4, help="tokens per step of the reference arm")
+    ap.add_argument("--cpu-tokens", type=int, default=512, help="tokens in the CPU-oracle baseline sample")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    ap.add_argument("--ref-tokens", type=int, default=0,
+                    help="tokens per step of the reference arm (0: sized so the run takes a few minutes)")
     ap.add_argument("--profile-case", action="store_true",
                     help="only build the layer and run warmup+steps forwards (the command ncu wraps)")
     ap.add_argument("--write-traffic", nargs=3, metavar=("KEY", "BYTES", "SOURCE"),
@@ -472,6 +588,8 @@ def main():
     from mixture_experts_layer_87_b300 import capi
     capi.lib()
     pk = peaks()
+    if rank == 0 or world > 1:
+        pk["fp8"] = measure_fp8_peak()
     clocks = ClockSampler()
     if args.workload == "decode":
         clocks.start()
@@ -497,45 +615,43 @@ def main():
     if not args.no_variants and args.workload == "v3":
         del layer, res["layer"]
         torch.cuda.empty_cache()
+        rm = measure(synth.get_config("mid"), args, world, pk)
+        variants["mid"] = variant_summary(rm)
+        del rm
+        torch.cuda.empty_cache()
         r8 = measure(synth.get_config("v3_fp8"), args, world, pk)
-        variants["v3_fp8"] = {"value": round(r8["value"], 1), "ms_per_step": round(r8["ms_per_step"], 4),
-                              "roofline": r8["roofline"], "layer_roofline_frac": round(r8["layer_roofline_frac"], 4),
-                              "stage_ms": {k: round(v, 4) for k, v in r8["stage_ms"].items()}}
+        variants["v3_fp8"] = variant_summary(r8)
         dec_layer = r8["layer"]
         del r8
-        dl = _retarget(dec_layer, synth.get_config("decode"))
-        dec = measure_decode(args, world, pk, dl)
+        dec = measure_decode(args, world, pk, dec_layer.with_tokens(synth.get_config("decode").T))
         variants["decode_fp8"] = {k: v for k, v in dec.items() if k != "per_step"}
-        del dec_layer, dl
+        del dec_layer
         torch.cuda.empty_cache()
 
     cpu = None
-    if rank == 0 and world == 1:
-        sample = np.arange(0, cfg.T, cfg.T // args.cpu_tokens)[:args.cpu_tokens]
-        secs = oracle_sample(cfg, res["u_host"], sample)
-        cpu = {"value": round(len(sample) / secs, 3), "unit": UNIT, "cores": host_cores(), "kind": "oracle",
-               "sample": f"{len(sample)} tokens (every {cfg.T // args.cpu_tokens}th) of the {cfg.T}-token batch: "
-                         f"routing + full layer output in the fp64 C oracle, input generation excluded"}
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline_leg(cfg, res["u_host"], args.cpu_tokens)
 
     if rank == 0:
+        conf = workload_config(cfg, world)
+        conf["max_over_mean_load"] = round(res["max_over_mean_load"], 3)
         line = {
             "metric": METRIC, "value": round(res["value"], 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(res["ms_per_step"], 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": cfg.prec, "data": "synthetic",
-            "config": {"workload": f"DeepSeek-V3-shaped MoE layer forward ({cfg.name}): T={cfg.T}, d={cfg.d}, "
-                                   f"{cfg.E} routed experts top-{cfg.k} + {cfg.n_shared} shared, I={cfg.inter}, "
-                                   f"{cfg.prec}, clustered tokens (max/mean load "
-                                   f"{res['max_over_mean_load']:.2f})",
-                       "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k, "n_shared": cfg.n_shared, "inter": cfg.inter,
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": "inputs larger than L2: every step streams the expert weights "
-                             f"({(cfg.E + cfg.n_shared) * 3 * cfg.d * cfg.inter * (2 if cfg.prec == 'bf16' else 1) / 1e9:.1f} GB)"},
+            "config": conf,
             "roofline": res["roofline"],
             "layer_roofline_frac": round(res["layer_roofline_frac"], 4),
+            "layer_bound": res["layer_bound"],
+            "layer_tflops": round(res["layer_tflops"], 1),
+            "peaks": {"bf16_burst_tflops": pk["bf16"], "bf16_sustained_tflops": pk["bf16_sus"],
+                      "fp8_measured_tflops": round(pk["fp8"], 1) if pk.get("fp8") else None,
+                      "hbm_gbs": pk["hbm"], "source": pk["source"]},
             "stage_ms": {k: round(v, 4) for k, v in res["stage_ms"].items()},
             "cpu_baseline": cpu,
             "e2e": {"value": round(world * cfg.T / (e2e_ms * 1e-3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h,
+                    "note": "copies of neighbouring steps overlap the forward on separate streams"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
             "variants": variants,
@@ -562,17 +678,6 @@ def profile_case(args):
                       "status": st}))
     if st != 0:
         sys.exit(1)
-
-
-def _retarget(layer, cfg):
-    """A decode-shaped view of an already loaded FP8 layer: same weights, T=256."""
-    from mixture_experts_layer_87_b300 import MoELayer, capi
-    view = MoELayer.__new__(MoELayer)
-    view.__dict__.update(layer.__dict__)
-    view.T = cfg.T
-    view.dims = capi.dims(cfg.T, cfg.d, cfg.E, cfg.k, cfg.n_shared, cfg.inter, cfg.prec)
-    view.ws = torch.empty(capi.moe_workspace_size(view.dims), dtype=torch.uint8, device="cuda")
-    return view
 
 
 if __name__ == "__main__":

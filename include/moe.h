@@ -145,8 +145,11 @@ moe_status moe_route(const moe_dims* dims, const uint16_t* u, const uint16_t* ce
  * Limits: T * E <= MOE_ROUTE_NOALLOC_MAX_LOGITS, else MOE_ERR_UNSUPPORTED is
  * returned and nothing is enqueued; other limits as moe_route.
  * Set-up: the first call on a device (the current device) looks up the
- * device address of the array with cudaGetSymbolAddress and caches it; make
- * that first call on each device before any stream capture begins.
+ * device address of the array with cudaGetSymbolAddress and caches it with
+ * the id of the device's current context; make that first call on each device
+ * before any stream capture begins.  If the context changes (cudaDeviceReset,
+ * or a context the caller made current), the next call on that device looks
+ * the address up again, so it is a set-up call too.
  * Sharing: every call on a device uses the same array, whose content is
  * whatever the last call left (every logit read is first written by the same
  * call).  Calls whose work overlaps on the GPU -- on different streams, or

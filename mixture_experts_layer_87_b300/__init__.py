@@ -13,8 +13,8 @@ from . import capi
 from .capi import (MoEError, moe_bias_update, moe_combine, moe_forward, moe_grouped_ffn,
                    moe_pack_gate_up, moe_permute, moe_quantize_fp8_blocks, moe_read_device_status,
                    moe_route, moe_route_noalloc, moe_selftest_wait_timeout, moe_workspace_size)
-from .layer import MoELayer
+from .layer import HostPipeline, MoELayer
 
-__all__ = ["capi", "MoEError", "MoELayer", "moe_bias_update", "moe_combine", "moe_forward", "moe_grouped_ffn",
+__all__ = ["capi", "HostPipeline", "MoEError", "MoELayer", "moe_bias_update", "moe_combine", "moe_forward", "moe_grouped_ffn",
            "moe_pack_gate_up", "moe_permute", "moe_quantize_fp8_blocks", "moe_read_device_status", "moe_route",
            "moe_route_noalloc", "moe_selftest_wait_timeout", "moe_workspace_size"]

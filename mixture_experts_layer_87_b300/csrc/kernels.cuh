@@ -84,9 +84,31 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   float sum = lane < k ? my_s : 0.0f;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  float gate = lane < k ? my_s / sum : 0.0f;
+  if (!(sum >= FLT_MIN)) {
+    // Every selected affinity underflowed (all their logits below about -87):
+    // s_j / sum_j' s_j' is still well defined, so take it in the log domain,
+    // g_j = exp(log s_j - m) / sum_j' exp(log s_j' - m), m = max log s, with
+    // log s = z - log(1 + e^z) from the selected expert's logit.  (sum is
+    // warp-uniform, so the whole warp takes this branch.)
+    float ls = -INFINITY;
+    if (lane < k && my_idx >= 0 && my_idx < E) {
+      float zz = z[(int64_t)t * E + my_idx];
+      for (int p = 1; p < splits; ++p) zz += z[p * split_stride + (int64_t)t * E + my_idx];
+      ls = zz < 0.0f ? zz - log1pf(expf(zz)) : -log1pf(expf(-zz));
+    }
+    float m = ls;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const float w = lane < k ? expf(ls - m) : 0.0f;
+    float wsum = w;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+    gate = w / wsum;
+  }
   if (lane < k) {
     idx_out[(int64_t)t * k + lane] = my_idx;
-    gate_out[(int64_t)t * k + lane] = my_s / sum;
+    gate_out[(int64_t)t * k + lane] = gate;
     atomicAdd(&counts[my_idx], 1);
     if (mask) atomicOr(&mask[(int64_t)my_idx * W + (t >> 5)], 1u << (t & 31));
   }

@@ -703,21 +703,61 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex scratch_mutex;
-float* scratch_addr[kMaxDevices] = {};
+struct ScratchCache {
+  unsigned long long ctx_id;  // unique id of the context the address belongs to (0: none yet)
+  float* addr;
+};
+ScratchCache scratch_cache[kMaxDevices] = {};
 
-// Device address of route_logits_scratch on the current device, looked up on
-// first use and cached.
+// Driver calls that identify the current context; every context of the
+// process has its own id, never reused, so a device reset (a new primary
+// context, whose copy of the array may sit elsewhere) is always noticed.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <class F>
+F driver_fn(const char* name, int version) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<F>(p);
+}
+
+moe_status current_ctx_id(unsigned long long* id) {
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent", 12000);
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId", 12000);
+  if (!get_current || !get_id) return MOE_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return MOE_ERR_CUDA;
+  *id = 0;
+  if (ctx && get_id(ctx, id) != CUDA_SUCCESS) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+// Device address of route_logits_scratch in the current device's current
+// context: looked up with cudaGetSymbolAddress the first time (which also
+// makes the device's primary context current if it was not) and cached per
+// device together with the context's id; looked up again whenever the
+// context has changed since (for instance after cudaDeviceReset).
 moe_status route_scratch(float** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(scratch_mutex);
-  if (!scratch_addr[dev]) {
+  unsigned long long id = 0;
+  MOE_TRY(current_ctx_id(&id));
+  ScratchCache& c = scratch_cache[dev];
+  if (id == 0 || c.ctx_id != id || !c.addr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, route_logits_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
-    scratch_addr[dev] = static_cast<float*>(p);
+    MOE_TRY(current_ctx_id(&id));
+    if (id == 0) return MOE_ERR_CUDA;
+    c.ctx_id = id;
+    c.addr = static_cast<float*>(p);
   }
-  *out = scratch_addr[dev];
+  *out = c.addr;
   return MOE_OK;
 }
 

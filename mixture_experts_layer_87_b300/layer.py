@@ -82,5 +82,65 @@ class MoELayer:
         capi.moe_forward(self.dims, self.weights(), u, bias, out, counts, self.ws, stream)
         return out
 
+    def with_tokens(self, T: int) -> "MoELayer":
+        """A layer of the same weights (shared, not copied) for batches of T
+        tokens, with its own workspace: e.g. the decode-shaped T=256 steps of a
+        layer loaded for 8192-token batches."""
+        view = MoELayer.__new__(MoELayer)
+        view.__dict__.update(self.__dict__)
+        view.T = T
+        view.dims = capi.dims(T, self.d, self.E, self.k, self.n_shared, self.inter, self.prec)
+        view.ws = torch.empty(capi.moe_workspace_size(view.dims), dtype=torch.uint8, device=self.device)
+        return view
+
     def status(self) -> int:
         return capi.moe_read_device_status(self.ws)
+
+
+class HostPipeline:
+    """The layer over batches that live in pinned host memory.
+
+    Batch i's copy to the device, batch i's forward and batch i's result copy
+    back run on three streams, with two device buffers each way, so the copy of
+    batch i+1 in and of batch i-1 out overlap the forward of batch i.  Every
+    batch still makes the whole round trip: u from host to device, h' from
+    device to host.  Batches run one forward at a time (the forwards share the
+    layer's workspace).
+    """
+
+    DEPTH = 2
+
+    def __init__(self, layer: MoELayer):
+        self.layer = layer
+        dev = layer.device
+        self.u = [torch.empty((layer.T, layer.d), dtype=torch.bfloat16, device=dev) for _ in range(self.DEPTH)]
+        self.out = [torch.empty((layer.T, layer.d), dtype=torch.bfloat16, device=dev) for _ in range(self.DEPTH)]
+        self.s_in, self.s_run, self.s_out = (torch.cuda.Stream(dev) for _ in range(3))
+        ev = lambda: [torch.cuda.Event() for _ in range(self.DEPTH)]
+        self.copied_in, self.computed, self.copied_out = ev(), ev(), ev()
+        self.used = [False] * self.DEPTH
+
+    def run(self, u_host, bias: torch.Tensor, out_host, after: torch.cuda.Stream | None = None) -> None:
+        """u_host, out_host: sequences of pinned [T, d] bf16 host tensors (the
+        same tensor may repeat).  The calling stream (or `after`) waits for the
+        last copy back before it continues."""
+        start = torch.cuda.current_stream() if after is None else after
+        self.s_in.wait_stream(start)
+        for i, (uh, oh) in enumerate(zip(u_host, out_host)):
+            b = i % self.DEPTH
+            if self.used[b]:
+                self.s_in.wait_event(self.computed[b])        # the forward that read u[b] is done
+            with torch.cuda.stream(self.s_in):
+                self.u[b].copy_(uh, non_blocking=True)
+                self.copied_in[b].record(self.s_in)
+            self.s_run.wait_event(self.copied_in[b])
+            if self.used[b]:
+                self.s_run.wait_event(self.copied_out[b])     # out[b] of two batches ago is on the host
+            self.layer.forward(self.u[b], bias, self.out[b], stream=self.s_run)
+            self.computed[b].record(self.s_run)
+            self.s_out.wait_event(self.computed[b])
+            with torch.cuda.stream(self.s_out):
+                oh.copy_(self.out[b], non_blocking=True)
+                self.copied_out[b].record(self.s_out)
+            self.used[b] = True
+        start.wait_stream(self.s_out)

@@ -242,6 +242,36 @@ def layer_output(u_bits: np.ndarray, tokens: np.ndarray, idx: np.ndarray, gate: 
     return out
 
 
+def expert_rows(u_bits: np.ndarray, tokens: np.ndarray, idx: np.ndarray, routed_weights, shared_weights,
+                n_shared: int, E: int, fp8: bool = False):
+    """The expert outputs layer_output sums, kept apart, fp64.
+
+    Returns (y [n, k, d], ysh [N_s, n, d]) for the n given tokens:
+    y[t, j] = FFN_{idx[t, j]}(x_t) and ysh[s, t] = FFN_s(x_t), with the same
+    operands as layer_output (fp8=True: u quantised per 1x128 tile, weights
+    per 128x128 block, h per 1x128 tile; ai.flicky.cc 3.3 items 1-2).
+    combine(u, ysh, y.reshape(n*k, d), slot=arange, gate) then assembles
+    h'_t of the layer equation (ai.flicky.cc 2.1.2).
+    """
+    tokens = np.asarray(tokens, np.int64)
+    u_rows = bf16_to_f64(u_bits[tokens])
+    x = fp8_roundtrip_1x128(u_rows) if fp8 else u_rows
+    n, k = idx.shape
+    d = u_rows.shape[1]
+    y = np.zeros((n, k, d))
+    ysh = np.zeros((n_shared, n, d))
+    for s in range(n_shared):
+        w1, w3, w2 = expert_operands(*shared_weights(s), fp8)
+        ysh[s] = swiglu(x, w1, w3, w2, h_quant=fp8)
+    for e in range(E):
+        rows, js = np.nonzero(idx == e)
+        if rows.size == 0:
+            continue
+        w1, w3, w2 = expert_operands(*routed_weights(e), fp8)
+        y[rows, js] = swiglu(x[rows], w1, w3, w2, h_quant=fp8)
+    return y, ysh
+
+
 def combine(u_bits: np.ndarray, shared_y: np.ndarray, y_perm: np.ndarray, slot: np.ndarray,
             gate: np.ndarray) -> np.ndarray:
     """out_t = u_t + sum_s shared_y[s, t] + sum_j gate[t, j] y_perm[slot[t, j]], fp64.

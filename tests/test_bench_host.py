@@ -45,3 +45,49 @@ def test_unreadable_file_falls_back_and_says_so(tmp_path):
         pk = bench.peaks(_write(tmp_path, bad))
         assert pk["source"].startswith("fallback (MEASURED_PEAKS.json unreadable")
         assert pk["hbm"] == 6400.0
+
+
+def test_tensor_peak_is_burst_bf16_and_measured_or_nominal_fp8():
+    import synth
+    pk = {"hbm": 6500.0, "bf16": 1716.2, "bf16_sus": 1354.8, "source": "measured"}
+    assert bench.tensor_peak(synth.get_config("v3"), pk)[0] == 1716.2
+    assert bench.tensor_peak(synth.get_config("v3_fp8"), pk)[0] == 2 * 1716.2      # fp8 not measured
+    pk["fp8"] = 3300.0
+    assert bench.tensor_peak(synth.get_config("v3_fp8"), pk)[0] == 3300.0
+    assert bench.tensor_peak(synth.get_config("v3"), pk)[0] == 1716.2
+
+
+def test_roofline_fraction_recomputes_from_the_peak():
+    """Both sides of the roofline recompute by hand from the algorithmic work,
+    the stage time and the peaks; frac is the slower side's."""
+    import numpy as np
+    import synth
+    cfg = synth.get_config("v3")
+    pk = {"hbm": 6500.0, "bf16": 1716.2, "bf16_sus": 1354.8, "source": "measured"}
+    counts = np.full(cfg.E, cfg.T * cfg.k // cfg.E, np.int32)
+    r = bench.roofline(cfg, {"routed_gate_up": 4.0}, counts, pk)
+    flops = 2 * cfg.T * cfg.k * cfg.d * 2 * cfg.inter
+    nbytes = cfg.E * 2 * cfg.inter * cfg.d * 2 + cfg.T * cfg.k * (cfg.d + cfg.inter) * 2
+    assert r["algorithmic_flops"] == flops and r["algorithmic_bytes"] == nbytes
+    assert abs(r["tensor_frac"] - flops / 4e-3 / 1e12 / 1716.2) < 1e-4
+    assert abs(r["hbm_frac"] - nbytes / 4e-3 / 1e9 / 6500.0) < 1e-4
+    assert r["frac"] == max(r["tensor_frac"], r["hbm_frac"])
+    assert r["bound"] == ("tensor" if r["tensor_frac"] >= r["hbm_frac"] else "hbm")
+    assert abs(r["frac_of_sustained_bf16"] - flops / 4e-3 / 1e12 / 1354.8) < 1e-4
+
+
+def test_both_arms_name_the_same_workload():
+    import synth
+    for name in ("v3", "v3_fp8", "mid"):
+        cfg = synth.get_config(name)
+        a, b = bench.workload_config(cfg), bench.workload_config(synth.get_config(name))
+        assert a == b and a["workload"].startswith(("DeepSeek-V3-shaped", "mid-sized"))
+
+
+def test_clock_sampler_without_a_gpu_id_reports_nothing():
+    s = bench.ClockSampler.__new__(bench.ClockSampler)
+    s.proc, s.uuid = None, None
+    s.start()
+    assert s.proc is None
+    out = s.stop()
+    assert out["sm_mhz"] is None and "not sampled" in out["reasons"][0]

@@ -18,7 +18,7 @@ import torch
 
 import synth
 from mixture_experts_layer_87_b300 import MoELayer, capi
-from parity import TOL
+from parity import TOL, Y_TOL
 from test_gpu_parity import _forward_parity
 
 pytestmark = pytest.mark.gpu
@@ -47,28 +47,28 @@ def test_empty_batch(prec):
 @pytest.mark.parametrize("name", ["tiny", "tiny_fp8"])
 def test_single_token(name):
     cfg = _cfg(name, T=1)
-    err, err_ffn = _forward_parity(cfg)
-    assert err <= TOL[cfg.prec] and err_ffn <= 2 * TOL[cfg.prec]
+    err, err_y = _forward_parity(cfg)
+    assert err <= TOL[cfg.prec] and err_y <= Y_TOL[cfg.prec]
 
 
 @pytest.mark.parametrize("prec", ["bf16", "fp8"])
 def test_one_expert_top1_no_shared_is_a_dense_swiglu(prec):
     cfg = _cfg("tiny", E=1, k=1, n_shared=0, prec=prec)
-    err, err_ffn = _forward_parity(cfg)
-    assert err <= TOL[cfg.prec] and err_ffn <= 2 * TOL[cfg.prec]
+    err, err_y = _forward_parity(cfg)
+    assert err <= TOL[cfg.prec] and err_y <= Y_TOL[cfg.prec]
 
 
 @pytest.mark.parametrize("name", ["ragged", "ragged_fp8"])
 def test_no_shared_expert(name):
     cfg = _cfg(name, n_shared=0)
-    err, err_ffn = _forward_parity(cfg)
-    assert err <= TOL[cfg.prec] and err_ffn <= 2 * TOL[cfg.prec]
+    err, err_y = _forward_parity(cfg)
+    assert err <= TOL[cfg.prec] and err_y <= Y_TOL[cfg.prec]
 
 
 def test_largest_routing_1024_experts_top32():
     cfg = _cfg("tiny", T=96, d=128, E=1024, k=32, n_shared=1, inter=128, bias="normal")
-    err, err_ffn = _forward_parity(cfg)
-    assert err <= TOL[cfg.prec] and err_ffn <= 2 * TOL[cfg.prec]
+    err, err_y = _forward_parity(cfg)
+    assert err <= TOL[cfg.prec] and err_y <= Y_TOL[cfg.prec]
 
 
 @pytest.mark.parametrize("prec", ["bf16", "fp8"])
@@ -83,10 +83,10 @@ def test_all_tokens_on_the_same_experts(prec):
     orig = synth.bias
     try:
         synth.bias = lambda c: host_bias.clone() if c.name == cfg.name else orig(c)
-        err, err_ffn = tp._forward_parity(cfg)
+        err, err_y = tp._forward_parity(cfg)
     finally:
         synth.bias = orig
-    assert err <= TOL[cfg.prec] and err_ffn <= 2 * TOL[cfg.prec]
+    assert err <= TOL[cfg.prec] and err_y <= Y_TOL[cfg.prec]
 
 
 @pytest.mark.parametrize("d,k", [(128, 32), (384, 31), (256, 16)])
@@ -110,3 +110,30 @@ def test_permute_copies_every_row(d, k):
     assert capi.moe_read_device_status(ws) == 0
     p = perm.long()
     assert torch.equal(x.view(torch.int16), u[p].view(torch.int16))
+
+
+def test_gates_when_every_selected_affinity_underflows():
+    """Logits near -150: every sigmoid affinity underflows to 0 in fp32, yet the
+    gates s_j / sum s (well defined in fp64) must come out finite, summing to
+    1, and equal to the oracle's for the GPU's (near-tie) selection."""
+    import oracle
+    from parity import check_selection
+    T, d, E, k = 8, 256, 16, 4
+    u = (1.0 + torch.arange(T, dtype=torch.float32)[:, None] / 16).expand(T, d).to(torch.bfloat16).contiguous()
+    c = (-(150.0 + 0.5 * torch.arange(E, dtype=torch.float32)[:, None]) / d).expand(E, d)
+    cent = c.to(torch.bfloat16).contiguous()
+    bias = torch.zeros(E, dtype=torch.float32)
+    dm = capi.dims(T, d, E, k, 0, 128, "bf16")
+    ws = torch.empty(capi.moe_workspace_size(dm), dtype=torch.uint8, device=DEV)
+    idx = torch.empty((T, k), dtype=torch.int32, device=DEV)
+    gate = torch.empty((T, k), dtype=torch.float32, device=DEV)
+    cnt = torch.empty(E, dtype=torch.int32, device=DEV)
+    capi.moe_route(dm, u.to(DEV), cent.to(DEV), bias.to(DEV), idx, gate, cnt, ws)
+    assert capi.moe_read_device_status(ws) == 0
+    idx, gate = idx.cpu().numpy(), gate.cpu().numpy()
+    r = oracle.route(synth.bf16_bits(u), synth.bf16_bits(cent), bias.numpy(), k, want_all=True)
+    assert (r["s_all"] < 1e-60).all() and (r["s_all"] > 0).all()     # underflows fp32, not fp64
+    check_selection(idx, r, bias.numpy(), k)
+    assert np.isfinite(gate).all()
+    np.testing.assert_allclose(gate.sum(1), 1.0, atol=1e-6)
+    np.testing.assert_allclose(gate, oracle.gates_for(r["s_all"], idx), rtol=0, atol=2e-6)

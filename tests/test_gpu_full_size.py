@@ -1,7 +1,17 @@
-"""Parity at the full V3 sizes, in the launch configuration the bench times:
-routing, counts and permutation of all 8192 tokens bit for bit (near-ties
-excepted), and the layer output on a strided sample of tokens (tokens are
-independent, so per-token parity is exact)."""
+"""Parity at the full sizes of the layer, in the launch configuration the bench
+times (T=8192, d=7168, 256 routed experts top-8 + 1 shared, I=2048, bf16 and
+FP8; and the decode-shaped FP8 stream, T=256 per step over 50 steps with the
+bias update between steps):
+  * routing, loads, offsets and permutation of every token bit for bit (near-
+    ties excepted: the GPU's pick must lie inside the near-tie set);
+  * h' and the routed expert outputs y_perm on a token sample that covers every
+    (expert, 128-row token chunk) work item of the grouped GEMMs, each expert's
+    last, ragged chunk included (tokens are independent, so per-token parity is
+    exact);
+  * decode: loads and the fp32 bias trajectory bit for bit at every one of the
+    50 steps, and h' and y_perm of all 256 tokens at steps 0, 24 and 49.
+The V3 FP8 layer and the decode stream share their weights (same seed), so one
+oracle pass over the 257 experts serves both."""
 import numpy as np
 import pytest
 import torch
@@ -9,89 +19,125 @@ import torch
 import oracle
 import synth
 from mixture_experts_layer_87_b300 import capi
-from parity import TOL, HostLayer, bf16_to_np, check_selection, ffn_rel_err, rel_err
+from parity import (TOL, Y_TOL, HostLayer, check_routing_and_dispatch, chunk_covering_tokens, gpu_layer_pass,
+                    gpu_rows, oracle_rows, rel_err)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
+DECODE_CHECKED_STEPS = (0, 24, 49)
 
 
-@pytest.mark.parametrize("name,n_sample", [("v3", 32), ("v3_fp8", 12)])
-def test_v3_forward_parity_sampled(name, n_sample):
-    cfg = synth.get_config(name)
+def _v3_pass(host, layer, cfg):
+    u = synth.tokens(cfg)
+    bias = np.asarray(host.bias)
+    res = gpu_layer_pass(layer, u.to(DEV), host.bias.to(DEV))
+    ub = synth.bf16_bits(u)
+    r = oracle.route(ub, synth.bf16_bits(host.cent), bias, cfg.k, want_all=True)
+    ties = check_routing_and_dispatch(res, r, bias, cfg.E, cfg.k)
+    # a strided base (every 128th token) plus whatever covers the remaining chunks
+    tokens = chunk_covering_tokens(res["idx"], cfg.E, base=np.arange(0, cfg.T, 128))
+    idx = res["idx"][tokens]
+    h, y = gpu_rows(res, tokens)
+    return dict(ties=ties, tokens=tokens, ub=ub[tokens], idx=idx, gate=oracle.gates_for(r["s_all"][tokens], idx),
+                h=h, y=y, max_over_mean=float(res["counts"].max() / (cfg.T * cfg.k / cfg.E)))
+
+
+def _decode_loop(host, layer):
+    """The 50-step decode stream on the GPU with the bias update between steps,
+    the oracle router beside it; loads and bias compared at every step."""
+    cfg = synth.get_config("decode")
+    cent = synth.bf16_bits(host.cent)
+    b_dev = torch.zeros(cfg.E, dtype=torch.float32, device=DEV)
+    b_ref = np.zeros(cfg.E, np.float32)
+    steps, ratios, n_ties = {}, [], 0
+    for step in range(cfg.steps):
+        u = synth.tokens(cfg, step=step)
+        res = gpu_layer_pass(layer, u.to(DEV), b_dev)
+        ub = synth.bf16_bits(u)
+        r = oracle.route(ub, cent, b_ref, cfg.k, want_all=True)
+        ties = check_routing_and_dispatch(res, r, b_ref, cfg.E, cfg.k)
+        n_ties += len(ties)
+        c_ref = np.bincount((res["idx"] if ties else r["idx"]).ravel(), minlength=cfg.E).astype(np.int32)
+        np.testing.assert_array_equal(res["counts"], c_ref, err_msg=f"loads, step {step}")
+        if step in DECODE_CHECKED_STEPS:
+            tokens = np.arange(cfg.T)
+            h, y = gpu_rows(res, tokens)
+            steps[step] = dict(ub=ub, idx=res["idx"], gate=oracle.gates_for(r["s_all"], res["idx"]), h=h, y=y)
+        capi.moe_bias_update(cfg.E, cfg.T, cfg.k, res["counts_dev"], cfg.gamma, b_dev)
+        b_ref = oracle.bias_update(c_ref, b_ref, cfg.T, cfg.k, cfg.gamma)
+        np.testing.assert_array_equal(b_dev.cpu().numpy(), b_ref, err_msg=f"bias after step {step}")
+        ratios.append(c_ref.max() / (cfg.T * cfg.k / cfg.E))
+    return dict(steps=steps, ratios=ratios, ties=n_ties)
+
+
+@pytest.fixture(scope="module")
+def v3_bf16():
+    cfg = synth.get_config("v3")
     host = HostLayer(cfg, keep_weights=False)
     layer = host.device_layer()
     layer.release_staging()
-    u = synth.tokens(cfg)
-    counts = torch.empty(cfg.E, dtype=torch.int32, device=DEV)
-    out = layer.forward(u.to(DEV), host.bias.to(DEV), counts=counts)
-    assert layer.status() == 0
-    # routing and dispatch of the whole batch
-    dm = layer.dims
-    idx = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=DEV)
-    gate = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=DEV)
-    cnt = torch.empty(cfg.E, dtype=torch.int32, device=DEV)
-    capi.moe_route(dm, u.to(DEV), layer.centroids, host.bias.to(DEV), idx, gate, cnt, layer.ws)
-    R = cfg.T * cfg.k
-    offsets = torch.empty(cfg.E + 1, dtype=torch.int32, device=DEV)
-    perm = torch.empty(R, dtype=torch.int32, device=DEV)
-    slot = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=DEV)
-    fp8 = cfg.prec == "fp8"
-    x = torch.empty((R, cfg.d), dtype=torch.uint8 if fp8 else torch.bfloat16, device=DEV)
-    xs = torch.empty((cfg.d // 128, R), dtype=torch.float32, device=DEV) if fp8 else None
-    capi.moe_permute(dm, idx, u.to(DEV), offsets, perm, slot, x, xs, layer.ws)
-    assert capi.moe_read_device_status(layer.ws) == 0
-    idx_np = idx.cpu().numpy()
-    ub = synth.bf16_bits(u)
-    r = oracle.route(ub, synth.bf16_bits(host.cent), np.asarray(host.bias), cfg.k, want_all=True)
-    ties = check_selection(idx_np, r, np.asarray(host.bias), cfg.k)
-    print(f"{name}: {len(ties)} near-tie tokens of {cfg.T}")
-    lay = oracle.dispatch_layout(idx_np, cfg.E)
-    np.testing.assert_array_equal(counts.cpu().numpy(), lay["counts"])
-    np.testing.assert_array_equal(offsets.cpu().numpy(), lay["offsets"])
-    np.testing.assert_array_equal(perm.cpu().numpy(), lay["perm"])
-    np.testing.assert_array_equal(slot.cpu().numpy(), lay["slot"])
-    # the layer output on a strided sample
-    sample = np.arange(0, cfg.T, cfg.T // n_sample)[:n_sample]
-    g = oracle.gates_for(r["s_all"][sample], idx_np[sample])
-    ref = oracle.layer_output(ub, sample, idx_np[sample], g, host.routed_bits, host.shared_bits, cfg.n_shared,
-                              cfg.E, fp8=fp8)
-    got = bf16_to_np(out)[sample]
-    uref = oracle.bf16_to_f64(ub[sample])
-    err, err_ffn = rel_err(got, ref), ffn_rel_err(got, ref, uref)
-    print(f"{name}: max|err|/rms h' = {err:.3e}, on h'-u = {err_ffn:.3e}")
-    assert err <= TOL[cfg.prec]
-    assert err_ffn <= 2 * TOL[cfg.prec]
+    v = _v3_pass(host, layer, cfg)
+    del layer
+    torch.cuda.empty_cache()
+    v["h_ref"], v["y_ref"] = oracle_rows(host, v["ub"], v["idx"], v["gate"])
+    return v
 
 
-def test_decode_loop_bias_trajectory():
-    """50 decode steps with the bias update between them: the fp32 bias
-    trajectory matches the oracle's bit for bit (on near-tie steps the
-    oracle takes the GPU's validated selection), and the load evens out."""
-    cfg = synth.get_config("decode", d=512, E=64, k=6, inter=256)
-    host = HostLayer(cfg)
+@pytest.fixture(scope="module")
+def v3_fp8_and_decode():
+    cfg = synth.get_config("v3_fp8")
+    host = HostLayer(cfg, keep_weights=False)
     layer = host.device_layer()
-    b_dev = torch.zeros(cfg.E, dtype=torch.float32, device=DEV)
-    b_ref = np.zeros(cfg.E, np.float32)
-    counts = torch.empty(cfg.E, dtype=torch.int32, device=DEV)
-    cent = synth.bf16_bits(host.cent)
-    ratios = []
-    for step in range(cfg.steps):
-        u = synth.tokens(cfg, step=step)
-        layer.forward(u.to(DEV), b_dev, counts=counts)
-        idx = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=DEV)
-        gate = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=DEV)
-        cnt = torch.empty(cfg.E, dtype=torch.int32, device=DEV)
-        capi.moe_route(layer.dims, u.to(DEV), layer.centroids, b_dev, idx, gate, cnt, layer.ws)
-        capi.moe_bias_update(cfg.E, cfg.T, cfg.k, counts, cfg.gamma, b_dev)
-        assert capi.moe_read_device_status(layer.ws) == 0
-        np.testing.assert_array_equal(cnt.cpu().numpy(), counts.cpu().numpy())
-        r = oracle.route(synth.bf16_bits(u), cent, b_ref, cfg.k, want_all=True)
-        idx_np = idx.cpu().numpy()
-        ties = check_selection(idx_np, r, b_ref, cfg.k)
-        sel = idx_np if ties else r["idx"]
-        c_ref = np.bincount(sel.ravel(), minlength=cfg.E).astype(np.int32)
-        np.testing.assert_array_equal(counts.cpu().numpy(), c_ref)
-        b_ref = oracle.bias_update(c_ref, b_ref, cfg.T, cfg.k, cfg.gamma)
-        np.testing.assert_array_equal(b_dev.cpu().numpy(), b_ref)
-        ratios.append(c_ref.max() / (cfg.T * cfg.k / cfg.E))
-    assert np.mean(ratios[-5:]) < np.mean(ratios[:5])
+    layer.release_staging()
+    v = _v3_pass(host, layer, cfg)
+    dec = _decode_loop(host, layer.with_tokens(synth.get_config("decode").T))
+    del layer
+    torch.cuda.empty_cache()
+    # one oracle pass over the experts for the V3 sample and the decode steps
+    parts = [v] + [dec["steps"][s] for s in DECODE_CHECKED_STEPS]
+    h_ref, y_ref = oracle_rows(host, np.concatenate([p["ub"] for p in parts]),
+                               np.concatenate([p["idx"] for p in parts]), np.concatenate([p["gate"] for p in parts]))
+    start = 0
+    for p in parts:
+        n = len(p["idx"])
+        p["h_ref"], p["y_ref"] = h_ref[start:start + n], y_ref[start:start + n]
+        start += n
+    return v, dec
+
+
+def _report(name, v):
+    err, err_y = rel_err(v["h"], v["h_ref"]), rel_err(v["y"], v["y_ref"])
+    print(f"{name}: {len(v['idx'])} tokens, max|err|/rms h' = {err:.3e}, routed y = {err_y:.3e}")
+    return err, err_y
+
+
+def test_v3_bf16_routing_and_chunk_covering_output(v3_bf16):
+    v = v3_bf16
+    print(f"v3: {len(v['ties'])} near-tie tokens of 8192, max/mean load {v['max_over_mean']:.2f}")
+    err, err_y = _report("v3", v)
+    assert err <= TOL["bf16"]
+    assert err_y <= Y_TOL["bf16"]
+
+
+def test_v3_fp8_routing_and_chunk_covering_output(v3_fp8_and_decode):
+    v, _ = v3_fp8_and_decode
+    print(f"v3_fp8: {len(v['ties'])} near-tie tokens of 8192")
+    err, err_y = _report("v3_fp8", v)
+    assert err <= TOL["fp8"]
+    assert err_y <= Y_TOL["fp8"]
+
+
+def test_decode_loads_and_bias_every_step(v3_fp8_and_decode):
+    """Checked inside the loop at each of the 50 steps; here the load evens out."""
+    _, dec = v3_fp8_and_decode
+    r = dec["ratios"]
+    print(f"decode: {dec['ties']} near-tie tokens over 50 steps; max/mean load {r[0]:.2f} -> {r[-1]:.2f}")
+    assert np.mean(r[-5:]) < np.mean(r[:5])
+
+
+@pytest.mark.parametrize("step", DECODE_CHECKED_STEPS)
+def test_decode_output_all_tokens(v3_fp8_and_decode, step):
+    _, dec = v3_fp8_and_decode
+    err, err_y = _report(f"decode step {step}", dec["steps"][step])
+    assert err <= TOL["fp8"]
+    assert err_y <= Y_TOL["fp8"]

@@ -366,3 +366,91 @@ def test_combine_matches_layer_assembly():
     ref = oracle.layer_output(ub, np.arange(cfg.T), r["idx"], r["gate"], lambda e: _bits(routed[e]),
                               lambda s: _bits(shared[s]), cfg.n_shared, cfg.E)
     np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12 * np.abs(ref).max())
+
+
+# ----------------------------------------------------------------------------
+# the FP8 layer against its own dense statement
+def test_e4m3_round_matches_exhaustive_search():
+    """The dense FP8 statement's vectorised rounding equals the exhaustive
+    nearest-value search, halfway cases and saturation included."""
+    rng = np.random.default_rng(21)
+    table = brute.e4m3_value_table()
+    pos = sorted(v for c, v in table.items() if c < 0x80)
+    mids = [(a + b) / 2 for a, b in zip(pos[:-1], pos[1:])]           # every halfway point
+    x = np.concatenate([rng.standard_normal(1500) * 40, rng.standard_normal(500) * 1e-3,
+                        np.array(mids), -np.array(mids[::7]), [448.0, 460.0, 1e6, -1e6, 0.0]])
+    got = brute.e4m3_round(x)
+    ref = np.array([brute.nearest_e4m3(float(v)) for v in x])
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("name", ["tiny_fp8", "ragged_fp8"])
+def test_fp8_layer_equals_dense_fp8_statement(name):
+    """layer_output(fp8=True) -- which operands are quantised, the residual,
+    the gates -- against the dense all-experts-then-mask FP8 statement."""
+    cfg = synth.get_config(name)
+    b = np.asarray(synth.normal_f32(4243, (cfg.E,), 0.02))
+    u, c, _, routed, shared = _tiny_layer(cfg)
+    r = oracle.route(synth.bf16_bits(u), synth.bf16_bits(c), b, cfg.k)
+    out = oracle.layer_output(synth.bf16_bits(u), np.arange(cfg.T), r["idx"], r["gate"],
+                              lambda e: _bits(routed[e]), lambda s: _bits(shared[s]), cfg.n_shared, cfg.E, fp8=True)
+    f = lambda ws: tuple(w.double().numpy() for w in ws)
+    dense = brute.dense_layer_fp8(u.double().numpy(), c.double().numpy(), b, cfg.k,
+                                  [f(w) for w in routed], [f(w) for w in shared])
+    np.testing.assert_allclose(r["gate"], np.take_along_axis(dense["g"], r["idx"].astype(np.int64), 1),
+                               rtol=0, atol=1e-15)
+    scale = np.abs(dense["out"]).max()
+    np.testing.assert_allclose(out, dense["out"], rtol=0, atol=1e-12 * scale)
+
+
+def test_fp8_dense_statement_catches_planted_assembly_slips(monkeypatch):
+    """Slips planted in the oracle's FP8 assembly move it far from the dense
+    statement, so the comparison above would catch them: a quantised residual,
+    shared experts on the unquantised u, h left unquantised, weights left
+    unquantised."""
+    cfg = synth.get_config("ragged_fp8")
+    b = np.asarray(synth.normal_f32(4243, (cfg.E,), 0.02))
+    u, c, _, routed, shared = _tiny_layer(cfg)
+    ub = synth.bf16_bits(u)
+    r = oracle.route(ub, synth.bf16_bits(c), b, cfg.k)
+    f = lambda ws: tuple(w.double().numpy() for w in ws)
+    dense = brute.dense_layer_fp8(u.double().numpy(), c.double().numpy(), b, cfg.k,
+                                  [f(w) for w in routed], [f(w) for w in shared])["out"]
+    scale = np.abs(dense).max()
+    args = (ub, np.arange(cfg.T), r["idx"], r["gate"], lambda e: _bits(routed[e]), lambda s: _bits(shared[s]),
+            cfg.n_shared, cfg.E)
+    good = oracle.layer_output(*args, fp8=True)
+    assert np.abs(good - dense).max() <= 1e-12 * scale
+    x = oracle.bf16_to_f64(ub)
+    slips = {"quantised residual": good - x + oracle.fp8_roundtrip_1x128(x)}
+    w_sh = oracle.expert_operands(*_bits(shared[0]), fp8=True)
+    slips["shared on unquantised u"] = (good - oracle.swiglu(oracle.fp8_roundtrip_1x128(x), *w_sh, h_quant=True)
+                                        + oracle.swiglu(x, *w_sh, h_quant=True))
+    real_swiglu, real_ops = oracle.swiglu, oracle.expert_operands
+    monkeypatch.setattr(oracle, "swiglu", lambda *a, h_quant=False: real_swiglu(*a, h_quant=False))
+    slips["h unquantised"] = oracle.layer_output(*args, fp8=True)
+    monkeypatch.setattr(oracle, "swiglu", real_swiglu)
+    monkeypatch.setattr(oracle, "expert_operands", lambda w1, w3, w2, fp8: real_ops(w1, w3, w2, False))
+    slips["weights unquantised"] = oracle.layer_output(*args, fp8=True)
+    for what, bad in slips.items():
+        assert np.abs(bad - dense).max() > 1e-4 * scale, what
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "tiny_fp8", "ragged_fp8"])
+def test_expert_rows_assemble_to_layer_output(name):
+    """expert_rows keeps the expert outputs apart; combined with the gates
+    they give layer_output (itself pinned to the dense statements)."""
+    cfg = synth.get_config(name)
+    u, c, b, routed, shared = _tiny_layer(cfg)
+    ub = synth.bf16_bits(u)
+    r = oracle.route(ub, synth.bf16_bits(c), np.asarray(b), cfg.k)
+    fp8 = cfg.prec == "fp8"
+    tokens = np.arange(0, cfg.T, 3)
+    args = (ub, tokens, r["idx"][tokens], r["gate"][tokens], lambda e: _bits(routed[e]),
+            lambda s: _bits(shared[s]), cfg.n_shared, cfg.E)
+    y, ysh = oracle.expert_rows(*args[:3], *args[4:], fp8=fp8)
+    n, k = len(tokens), cfg.k
+    got = oracle.combine(ub[tokens], ysh, y.reshape(n * k, cfg.d), np.arange(n * k).reshape(n, k),
+                         r["gate"][tokens])
+    ref = oracle.layer_output(*args, fp8=fp8)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12 * np.abs(ref).max())
