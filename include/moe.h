@@ -63,10 +63,19 @@ typedef enum { MOE_BF16 = 0, MOE_FP8_E4M3 = 1 } moe_precision;
 
 /* Layer shape.  T tokens, hidden size d, E routed experts, k of them per
  * token, n_shared shared experts, SwiGLU intermediate size inter (= I) of
- * every expert, prec the precision of the expert GEMMs. */
+ * every expert, prec the precision of the expert GEMMs.
+ * Node-limited routing (ai.flicky.cc 2.1.2: a token is sent to at most 4
+ * nodes): route_groups > 0 places the experts on route_groups nodes of
+ * E / route_groups consecutive experts, and a token's k experts span at most
+ * route_group_limit of them -- the k best experts (biased score) on the
+ * route_group_limit nodes whose best expert scores highest.  0 and 0: no
+ * limit.  Requires E % route_groups == 0, route_groups <= 32,
+ * 1 <= route_group_limit <= route_groups and route_group_limit * E /
+ * route_groups >= k. */
 typedef struct {
   int32_t T, d, E, k, n_shared, inter;
   int32_t prec; /* moe_precision */
+  int32_t route_groups, route_group_limit;
 } moe_dims;
 
 /*

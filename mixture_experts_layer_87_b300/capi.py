@@ -35,7 +35,8 @@ class MoEError(RuntimeError):
 
 class moe_dims(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
-                ("n_shared", ctypes.c_int32), ("inter", ctypes.c_int32), ("prec", ctypes.c_int32)]
+                ("n_shared", ctypes.c_int32), ("inter", ctypes.c_int32), ("prec", ctypes.c_int32),
+                ("route_groups", ctypes.c_int32), ("route_group_limit", ctypes.c_int32)]
 
 
 class moe_weights(ctypes.Structure):
@@ -108,9 +109,10 @@ def _stream(stream):
     return stream
 
 
-def dims(T, d, E, k, n_shared, inter, prec) -> moe_dims:
+def dims(T, d, E, k, n_shared, inter, prec, route_groups=0, route_group_limit=0) -> moe_dims:
     p = {"bf16": MOE_BF16, "fp8": MOE_FP8_E4M3}.get(prec, prec)
-    return moe_dims(int(T), int(d), int(E), int(k), int(n_shared), int(inter), int(p))
+    return moe_dims(int(T), int(d), int(E), int(k), int(n_shared), int(inter), int(p), int(route_groups),
+                    int(route_group_limit))
 
 
 # ---------------------------------------------------------------- entry points

@@ -22,12 +22,18 @@ namespace moe {
 // descending, ties to the lower index) pick the experts; the gates are the
 // selected unbiased s divided by their sum.  Lane j keeps the j-th pick.
 // A NaN score ranks as -inf.
+// Node limit (the same section: a token is sent to at most 4 nodes): with
+// group_size > 0 the experts sit on nodes of group_size consecutive experts,
+// and once group_limit nodes are in use the arg-max only looks at experts on
+// those nodes -- the k best experts on the group_limit nodes whose best expert
+// scores highest.
 template <int VPL>
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ z, int splits,
+__global__ void __launch_bounds__(256, 1) route_topk_kernel(const float* __restrict__ z, int splits,
                                                          int64_t split_stride, int T, int E, int k,
                                                          const float* __restrict__ bias, int32_t* __restrict__ idx_out,
                                                          float* __restrict__ gate_out, int32_t* __restrict__ counts,
-                                                         uint32_t* __restrict__ mask, int W) {
+                                                         uint32_t* __restrict__ mask, int W, int group_size,
+                                                         int group_limit) {
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -52,13 +58,27 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   }
   int my_idx = -1;
   float my_s = 0.0f;
+  uint32_t nodes = 0;           // nodes in use (group_size > 0; at most 32 nodes)
+  uint32_t allowed = ~0u;       // bit j: expert lane + 32 j may still be picked
+  bool restricted = false;
   for (int r = 0; r < k; ++r) {
     float best = -INFINITY, bs = 0.0f;
     int bi = INT_MAX;
+    if (group_size > 0 && !restricted && __popc(nodes) >= group_limit) {
+      // the node budget is spent: from now on only experts on the used nodes
+      // (the set of nodes cannot change any more)
+      restricted = true;
+      allowed = 0;
+#pragma unroll 1
+      for (int j = 0; j < VPL; ++j) {
+        const int e = lane + 32 * j;
+        if (e < E && ((nodes >> (e / group_size)) & 1u)) allowed |= 1u << j;
+      }
+    }
 #pragma unroll
     for (int j = 0; j < VPL; ++j) {
       const int e = lane + 32 * j;
-      if (!((taken >> j) & 1u) && (sc[j] > best || (sc[j] == best && e < bi))) {
+      if (!(((taken | ~allowed) >> j) & 1u) && (sc[j] > best || (sc[j] == best && e < bi))) {
         best = sc[j];
         bi = e;
         bs = sv[j];
@@ -76,6 +96,7 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
       }
     }
     if (bi < E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (group_size > 0 && bi < E) nodes |= 1u << (bi / group_size);  // bi is the same in every lane
     if (lane == r) {
       my_idx = bi;
       my_s = bs;
@@ -290,38 +311,44 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
       }
     }
   } else {
+    // A quarter-warp (8 lanes) per 128-wide tile, 16 elements per lane: a
+    // lane reads 32 contiguous bytes of u and writes its 16 codes with one
+    // 16-byte store per destination row (a warp: 512 contiguous bytes).
     const int groups = d / 128;
-    const int hl = lane & 15, hw = lane >> 4;  // half-warp: one 128-wide tile
-    for (int g0 = 0; g0 < groups; g0 += 2) {
-      const int g = g0 + hw;
+    const int ql = lane & 7, qw = lane >> 3;
+    for (int g0 = 0; g0 < groups; g0 += 4) {
+      const int g = g0 + qw;
       const bool active = g < groups;
-      float f[8];
+      float f0[8], f1[8];
       float amax = 0.0f;
       if (active) {
-        unpack8(src[g * 16 + hl], f);
+        unpack8(src[g * 16 + 2 * ql], f0);
+        unpack8(src[g * 16 + 2 * ql + 1], f1);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(f0[i]), fabsf(f1[i])));
       }
 #pragma unroll
-      for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      for (int off = 4; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
       const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
-      uint2 code = make_uint2(0, 0);
+      uint4 code = make_uint4(0, 0, 0, 0);
       if (active) {
-        uint32_t c4[4];
+        uint32_t c8[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) c4[i] = e4m3x2(f[2 * i] / scale, f[2 * i + 1] / scale);
-        code.x = c4[0] | (c4[1] << 16);
-        code.y = c4[2] | (c4[3] << 16);
+        for (int i = 0; i < 4; ++i) {
+          c8[i] = e4m3x2(f0[2 * i] / scale, f0[2 * i + 1] / scale);
+          c8[4 + i] = e4m3x2(f1[2 * i] / scale, f1[2 * i + 1] / scale);
+        }
+        code = make_uint4(c8[0] | (c8[1] << 16), c8[2] | (c8[3] << 16), c8[4] | (c8[5] << 16), c8[6] | (c8[7] << 16));
         if (uq) {
-          reinterpret_cast<uint2*>(uq + (int64_t)t * d + g * 128)[hl] = code;
-          if (hl == 0) uq_scale[(int64_t)g * T + t] = scale;
+          reinterpret_cast<uint4*>(uq + (int64_t)t * d + g * 128)[ql] = code;
+          if (ql == 0) uq_scale[(int64_t)g * T + t] = scale;
         }
       }
       for (int j = 0; j < k; ++j) {
         const int s = __shfl_sync(0xffffffffu, my_slot, j);
         if (active && s >= 0) {
-          reinterpret_cast<uint2*>(static_cast<uint8_t*>(x_perm) + (int64_t)s * d + g * 128)[hl] = code;
-          if (hl == 0) x_scale[(int64_t)g * rows + s] = scale;
+          reinterpret_cast<uint4*>(static_cast<uint8_t*>(x_perm) + (int64_t)s * d + g * 128)[ql] = code;
+          if (ql == 0) x_scale[(int64_t)g * rows + s] = scale;
         }
       }
     }

@@ -116,6 +116,13 @@ moe_status check_dims(const moe_dims* d) {
   if (d->d % 128 != 0 || d->inter % 128 != 0) return MOE_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(d->T) * d->k > (int64_t(1) << 30)) return MOE_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(d->n_shared) * d->T > (int64_t(1) << 30)) return MOE_ERR_UNSUPPORTED;
+  if (d->route_groups < 0 || d->route_group_limit < 0) return MOE_ERR_INVALID_ARG;
+  if (d->route_groups > 0) {
+    if (d->route_groups > 32) return MOE_ERR_UNSUPPORTED;
+    if (d->E % d->route_groups != 0 || d->route_group_limit < 1 || d->route_group_limit > d->route_groups ||
+        int64_t(d->route_group_limit) * (d->E / d->route_groups) < d->k)
+      return MOE_ERR_INVALID_ARG;
+  }
   return MOE_OK;
 }
 
@@ -219,7 +226,8 @@ moe_status enqueue_route(const moe_dims& d, const uint16_t* u, const uint16_t* c
   const int vpl = (d.E + 31) / 32;
 #define MOE_TOPK(V)                                                                                              \
   route_topk_kernel<V><<<blocks, 256, 0, st>>>(z, sp.splits, a.split_stride, d.T, d.E, d.k, bias, idx, gate, counts, \
-                                               mask, W)
+                                               mask, W, d.route_groups > 0 ? d.E / d.route_groups : 0,            \
+                                               d.route_group_limit)
   if (vpl <= 1) MOE_TOPK(1);
   else if (vpl <= 2) MOE_TOPK(2);
   else if (vpl <= 4) MOE_TOPK(4);

@@ -16,11 +16,13 @@ from . import capi
 
 class MoELayer:
     def __init__(self, T: int, d: int, E: int, k: int, n_shared: int, inter: int, prec: str = "bf16",
-                 device: str | torch.device = "cuda"):
+                 device: str | torch.device = "cuda", route_groups: int = 0, route_group_limit: int = 0):
+        """route_groups, route_group_limit: node-limited routing (moe_dims)."""
         self.T, self.d, self.E, self.k, self.n_shared, self.inter, self.prec = T, d, E, k, n_shared, inter, prec
+        self.route_groups, self.route_group_limit = route_groups, route_group_limit
         self.device = torch.device(device)
         self.fp8 = prec == "fp8"
-        self.dims = capi.dims(T, d, E, k, n_shared, inter, prec)
+        self.dims = capi.dims(T, d, E, k, n_shared, inter, prec, route_groups, route_group_limit)
         self.ws = torch.empty(capi.moe_workspace_size(self.dims), dtype=torch.uint8, device=self.device)
         wt = torch.uint8 if self.fp8 else torch.bfloat16
         dev = self.device
@@ -89,7 +91,8 @@ class MoELayer:
         view = MoELayer.__new__(MoELayer)
         view.__dict__.update(self.__dict__)
         view.T = T
-        view.dims = capi.dims(T, self.d, self.E, self.k, self.n_shared, self.inter, self.prec)
+        view.dims = capi.dims(T, self.d, self.E, self.k, self.n_shared, self.inter, self.prec, self.route_groups,
+                              self.route_group_limit)
         view.ws = torch.empty(capi.moe_workspace_size(view.dims), dtype=torch.uint8, device=self.device)
         return view
 

@@ -50,6 +50,7 @@ def _load():
         i64, i32, vp, f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_float
         lib.oracle_bf16_to_f64.argtypes = [i64, vp, vp]
         lib.oracle_route.argtypes = [i64, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.oracle_route_limited.argtypes = [i64, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_decode.restype = ctypes.c_double
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
@@ -78,24 +79,30 @@ def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
 
 # ----------------------------------------------------------------------------
 # router
-def route(u_bits: np.ndarray, cent_bits: np.ndarray, bias: np.ndarray, k: int, want_all: bool = False):
+def route(u_bits: np.ndarray, cent_bits: np.ndarray, bias: np.ndarray, k: int, want_all: bool = False,
+          groups: int = 0, group_limit: int = 0):
     """Sigmoid affinities, biased top-k, normalised gates (ai.flicky.cc 2.1.2).
 
     u_bits [T, d] and cent_bits [E, d] are bf16 bit patterns, bias [E] fp32.
+    groups > 0: the experts sit on `groups` nodes of E/groups consecutive
+    experts and a token's k experts may span at most `group_limit` of them
+    (the same section: a token is sent to at most 4 nodes).
     Returns dict(idx [T,k] int32, s_sel [T,k], gate [T,k], gap [T], s_all [T,E]|None).
     """
     u_bits, cent_bits, bias = _c(u_bits, np.uint16), _c(cent_bits, np.uint16), _c(bias, np.float32)
     T, d = u_bits.shape
     E = cent_bits.shape[0]
     assert cent_bits.shape[1] == d and bias.shape == (E,) and 1 <= k <= E
+    if groups:
+        assert E % groups == 0 and 1 <= group_limit <= groups and group_limit * (E // groups) >= k
     idx = np.empty((T, k), np.int32)
     s_sel = np.empty((T, k), np.float64)
     gate = np.empty((T, k), np.float64)
     gap = np.empty(T, np.float64)
     s_all = np.empty((T, E), np.float64) if want_all else None
-    _load().oracle_route(T, d, E, k, u_bits.ctypes.data, cent_bits.ctypes.data, bias.ctypes.data,
-                         idx.ctypes.data, s_sel.ctypes.data, gate.ctypes.data, gap.ctypes.data,
-                         None if s_all is None else s_all.ctypes.data)
+    _load().oracle_route_limited(T, d, E, k, int(groups), int(group_limit), u_bits.ctypes.data,
+                                 cent_bits.ctypes.data, bias.ctypes.data, idx.ctypes.data, s_sel.ctypes.data,
+                                 gate.ctypes.data, gap.ctypes.data, None if s_all is None else s_all.ctypes.data)
     return dict(idx=idx, s_sel=s_sel, gate=gate, gap=gap, s_all=s_all)
 
 

@@ -172,3 +172,17 @@ def nearest_e4m3(x: float) -> float:
         if best is None or dist < best[0] or (dist == best[0] and (code & 1) == 0):
             best = (dist, code, v)
     return math.copysign(best[2], x)
+
+
+def node_limited_topk(score: np.ndarray, k: int, groups: int, limit: int) -> list:
+    """The k selected experts of one token when its experts may span at most
+    `limit` of `groups` nodes (E/groups consecutive experts per node), written
+    as: rank the nodes by their best expert (ties: the node of the lower expert
+    index), keep the first `limit`, then take the k best experts on those nodes
+    (ties: lower index).  Python sorts only."""
+    E = len(score)
+    gs = E // groups
+    best = [max(range(n * gs, (n + 1) * gs), key=lambda i: (score[i], -i)) for n in range(groups)]
+    nodes = sorted(range(groups), key=lambda n: (-score[best[n]], best[n]))[:limit]
+    allowed = [i for i in range(E) if i // gs in nodes]
+    return sorted(allowed, key=lambda i: (-score[i], i))[:k]

@@ -60,13 +60,30 @@ static int better(double a, int ia, double b, int ib) {
   return ia < ib;
 }
 
-void oracle_route(int64_t T, int d, int E, int k, const uint16_t* u, const uint16_t* cent,
-                  const float* bias, int32_t* idx, double* s_sel, double* gate, double* gap,
-                  double* s_all) {
+/*
+ * Node-limited routing (ai.flicky.cc 2.1.2: a token is sent to at most 4
+ * nodes).  The E experts sit on `groups` nodes of E / groups consecutive
+ * experts; groups == 0 means no limit.  The pages fix only the limit, not how
+ * the nodes are chosen; reading: the k experts are taken in biased-score
+ * order, and an expert is skipped when its node is not yet in use and `limit`
+ * nodes already are -- which keeps the `limit` nodes whose best expert scores
+ * highest and takes the k best experts inside them.  With a binding limit the
+ * near-tie distance also covers the choice of nodes: gap is at most the score
+ * of the pick that brought in the last node minus the best score on a node
+ * left out.
+ */
+void oracle_route_limited(int64_t T, int d, int E, int k, int groups, int limit, const uint16_t* u,
+                          const uint16_t* cent, const float* bias, int32_t* idx, double* s_sel, double* gate,
+                          double* gap, double* s_all) {
+  const int gs = groups > 0 ? E / groups : E;
 #pragma omp parallel for schedule(dynamic, 16)
   for (int64_t t = 0; t < T; ++t) {
     double s[E], score[E];
     char taken[E];
+    char used[groups > 0 ? groups : 1];
+    int n_used = 0;
+    double last_node_pick = INFINITY;
+    for (int n = 0; n < (groups > 0 ? groups : 1); ++n) used[n] = 0;
     for (int i = 0; i < E; ++i) {
       double z = 0.0;
       for (int c = 0; c < d; ++c) z += bf16_to_f64(u[t * d + c]) * bf16_to_f64(cent[(int64_t)i * d + c]);
@@ -78,20 +95,41 @@ void oracle_route(int64_t T, int d, int E, int k, const uint16_t* u, const uint1
     double sum = 0.0, kth = 0.0;
     for (int j = 0; j < k; ++j) {
       int best = -1;
-      for (int i = 0; i < E; ++i)
-        if (!taken[i] && (best < 0 || better(score[i], i, score[best], best))) best = i;
+      for (int i = 0; i < E; ++i) {
+        const int allowed = groups == 0 || used[i / gs] || n_used < limit;
+        if (!taken[i] && allowed && (best < 0 || better(score[i], i, score[best], best))) best = i;
+      }
       taken[best] = 1;
+      if (groups > 0 && !used[best / gs]) {
+        used[best / gs] = 1;
+        ++n_used;
+        last_node_pick = score[best];
+      }
       idx[t * k + j] = best;
       s_sel[t * k + j] = s[best];
       sum += s[best];
       kth = score[best];
     }
     for (int j = 0; j < k; ++j) gate[t * k + j] = s_sel[t * k + j] / sum;
-    int next = -1;
-    for (int i = 0; i < E; ++i)
-      if (!taken[i] && (next < 0 || better(score[i], i, score[next], next))) next = i;
-    gap[t] = next < 0 ? INFINITY : kth - score[next];
+    int next = -1, out = -1;
+    for (int i = 0; i < E; ++i) {
+      if (taken[i]) continue;
+      if (groups == 0 || used[i / gs] || n_used < limit) {
+        if (next < 0 || better(score[i], i, score[next], next)) next = i;
+      } else if (out < 0 || better(score[i], i, score[out], out)) {
+        out = i;
+      }
+    }
+    double g = next < 0 ? INFINITY : kth - score[next];
+    if (out >= 0 && last_node_pick - score[out] < g) g = last_node_pick - score[out];
+    gap[t] = g;
   }
+}
+
+void oracle_route(int64_t T, int d, int E, int k, const uint16_t* u, const uint16_t* cent,
+                  const float* bias, int32_t* idx, double* s_sel, double* gate, double* gap,
+                  double* s_all) {
+  oracle_route_limited(T, d, E, k, 0, 0, u, cent, bias, idx, s_sel, gate, gap, s_all);
 }
 
 /* ---------------------------------------------------------------------------

@@ -107,6 +107,8 @@ class LayerConfig:
     steps: int = 1             # >1: decode loop with the bias update between steps
     gamma: float = 0.001       # bias update speed
     seed: int = 0
+    route_groups: int = 0      # >0: experts on this many nodes of E/route_groups consecutive experts ...
+    route_group_limit: int = 0 # ... and a token's experts on at most this many of them
 
     @property
     def rows(self) -> int:
@@ -149,6 +151,10 @@ CONFIGS = {
     # of 256 tokens over 256 experts) with 32 experts, for profiling.
     "decode_slice": LayerConfig("decode_slice", T=32, d=7168, E=32, k=8, n_shared=1, inter=2048,
                                 prec="fp8", bias="zero", rho=V3_RHO, alpha=DECODE_ALPHA),
+    # V3 with node-limited routing: 256 experts on 8 nodes of 32, a token's 8
+    # experts on at most 4 nodes.
+    "v3_nodes": LayerConfig("v3_nodes", T=8192, d=7168, E=256, k=8, n_shared=1, inter=2048,
+                            rho=V3_RHO, alpha=V3_ALPHA, route_groups=8, route_group_limit=4),
     # Small parity shapes: several M/N/K tiles, ragged tails, odd expert counts.
     "ragged": LayerConfig("ragged", T=300, d=384, E=20, k=3, n_shared=1, inter=256,
                           rho=0.3, alpha=1.0),

@@ -57,7 +57,8 @@ class HostLayer:
 
     def device_layer(self, T=None) -> MoELayer:
         c = self.cfg
-        layer = MoELayer(c.T if T is None else T, c.d, c.E, c.k, c.n_shared, c.inter, c.prec)
+        layer = MoELayer(c.T if T is None else T, c.d, c.E, c.k, c.n_shared, c.inter, c.prec,
+                         route_groups=c.route_groups, route_group_limit=c.route_group_limit)
         layer.set_centroids(self.cent)
         for e in range(c.E):
             layer.load_expert(e, *self.routed(e))
@@ -66,19 +67,29 @@ class HostLayer:
         return layer
 
 
-def check_selection(idx_gpu: np.ndarray, r: dict, bias: np.ndarray, k: int):
+def check_selection(idx_gpu: np.ndarray, r: dict, bias: np.ndarray, k: int, groups: int = 0, limit: int = 0):
     """GPU selection vs oracle: identical sets except on near-tie tokens, where
     the GPU may pick any experts within NEAR_TIE of the k-th score (and must
-    keep every expert clearly above it).  Returns the near-tie token list."""
+    keep every expert clearly above it).  With node-limited routing (groups >
+    0) every selection spans at most `limit` nodes, and a near-tie selection
+    must score within k * NEAR_TIE of the oracle's in total (a tie between two
+    nodes can swap every expert of one for the other's).  Returns the near-tie
+    token list."""
     T = idx_gpu.shape[0]
     score = r["s_all"] + bias.astype(np.float64)[None, :]
+    gs = score.shape[1] // groups if groups else 0
     ties = []
     for t in range(T):
         g = sorted(idx_gpu[t].tolist())
         o = sorted(r["idx"][t].tolist())
         assert len(set(g)) == k, f"token {t}: duplicate experts {g}"
+        if groups:
+            assert len({e // gs for e in g}) <= limit, f"token {t}: experts {g} on more than {limit} nodes"
         if r["gap"][t] >= NEAR_TIE:
             assert g == o, f"token {t}: gpu {g} oracle {o} gap {r['gap'][t]}"
+        elif groups:
+            ties.append(t)
+            assert score[t, g].sum() >= score[t, o].sum() - k * NEAR_TIE, f"token {t}: gpu pick far from the best"
         else:
             ties.append(t)
             kth = score[t, r["idx"][t, -1]]
@@ -155,11 +166,12 @@ def gpu_layer_pass(layer: MoELayer, u_dev: torch.Tensor, bias_dev: torch.Tensor)
                 slot=slot.cpu().numpy())
 
 
-def check_routing_and_dispatch(res: dict, r: dict, bias: np.ndarray, E: int, k: int) -> list:
+def check_routing_and_dispatch(res: dict, r: dict, bias: np.ndarray, E: int, k: int, groups: int = 0,
+                               limit: int = 0) -> list:
     """Selection against the oracle (near-ties excepted), and the loads,
     offsets, permutation and slots of the GPU's own selection bit for bit
     against the oracle's canonical dropless layout.  Returns the near-ties."""
-    ties = check_selection(res["idx"], r, bias, k)
+    ties = check_selection(res["idx"], r, bias, k, groups, limit)
     np.testing.assert_array_equal(res["counts"], res["cnt"])
     lay = oracle.dispatch_layout(res["idx"], E)
     np.testing.assert_array_equal(res["counts"], lay["counts"])

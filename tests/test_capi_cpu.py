@@ -54,6 +54,12 @@ def _dims(**kw):
     (dict(inter=100), 2),      # I % 128
     (dict(T=-1), 1),
     (dict(prec=7), 1),
+    (dict(route_groups=3, route_group_limit=1), 1),    # E % groups
+    (dict(route_groups=4, route_group_limit=0), 1),    # limit < 1
+    (dict(route_groups=4, route_group_limit=5), 1),    # limit > groups
+    (dict(route_groups=8, route_group_limit=1), 1),    # 1 node of 2 experts < k = 4
+    (dict(E=64, route_groups=64, route_group_limit=4), 2),  # more than 32 nodes
+    (dict(route_groups=-1), 1),
 ])
 def test_workspace_size_rejects_bad_dims(lib, kw, code):
     n = ctypes.c_size_t(0)

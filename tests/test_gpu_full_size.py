@@ -32,8 +32,9 @@ def _v3_pass(host, layer, cfg):
     bias = np.asarray(host.bias)
     res = gpu_layer_pass(layer, u.to(DEV), host.bias.to(DEV))
     ub = synth.bf16_bits(u)
-    r = oracle.route(ub, synth.bf16_bits(host.cent), bias, cfg.k, want_all=True)
-    ties = check_routing_and_dispatch(res, r, bias, cfg.E, cfg.k)
+    r = oracle.route(ub, synth.bf16_bits(host.cent), bias, cfg.k, want_all=True, groups=cfg.route_groups,
+                     group_limit=cfg.route_group_limit)
+    ties = check_routing_and_dispatch(res, r, bias, cfg.E, cfg.k, cfg.route_groups, cfg.route_group_limit)
     # a strided base (every 128th token) plus whatever covers the remaining chunks
     tokens = chunk_covering_tokens(res["idx"], cfg.E, base=np.arange(0, cfg.T, 128))
     idx = res["idx"][tokens]
@@ -133,6 +134,33 @@ def test_decode_loads_and_bias_every_step(v3_fp8_and_decode):
     r = dec["ratios"]
     print(f"decode: {dec['ties']} near-tie tokens over 50 steps; max/mean load {r[0]:.2f} -> {r[-1]:.2f}")
     assert np.mean(r[-5:]) < np.mean(r[:5])
+
+
+def test_v3_node_limited_routing():
+    """256 experts on 8 nodes of 32, a token on at most 4 of them (the pages'
+    limit): the selection of all 8192 tokens against the oracle's node-limited
+    rule, the loads bit for bit."""
+    cfg = synth.get_config("v3_nodes")
+    u, cent, bias = synth.tokens(cfg), synth.centroids(cfg), synth.bias(cfg)
+    dm = capi.dims(cfg.T, cfg.d, cfg.E, cfg.k, cfg.n_shared, cfg.inter, cfg.prec, cfg.route_groups,
+                   cfg.route_group_limit)
+    ws = torch.empty(capi.moe_workspace_size(dm), dtype=torch.uint8, device=DEV)
+    idx = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=DEV)
+    gate = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=DEV)
+    cnt = torch.empty(cfg.E, dtype=torch.int32, device=DEV)
+    capi.moe_route(dm, u.to(DEV), cent.to(DEV), bias.to(DEV), idx, gate, cnt, ws)
+    assert capi.moe_read_device_status(ws) == 0
+    idx, gate, cnt = idx.cpu().numpy(), gate.cpu().numpy(), cnt.cpu().numpy()
+    r = oracle.route(synth.bf16_bits(u), synth.bf16_bits(cent), np.asarray(bias), cfg.k, want_all=True,
+                     groups=cfg.route_groups, group_limit=cfg.route_group_limit)
+    from parity import check_selection
+    ties = check_selection(idx, r, np.asarray(bias), cfg.k, cfg.route_groups, cfg.route_group_limit)
+    free = oracle.route(synth.bf16_bits(u), synth.bf16_bits(cent), np.asarray(bias), cfg.k)
+    changed = int((np.sort(free["idx"], 1) != np.sort(r["idx"], 1)).any(1).sum())
+    print(f"v3_nodes: {len(ties)} near-tie tokens; the node limit changed {changed} of {cfg.T} selections")
+    np.testing.assert_array_equal(cnt, np.bincount(idx.ravel(), minlength=cfg.E))
+    np.testing.assert_allclose(gate, oracle.gates_for(r["s_all"], idx), rtol=0, atol=2e-6)
+    assert changed > 0
 
 
 @pytest.mark.parametrize("step", DECODE_CHECKED_STEPS)

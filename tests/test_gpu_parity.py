@@ -16,7 +16,8 @@ DEV = "cuda"
 
 
 def _ws(cfg, T=None):
-    dm = capi.dims(cfg.T if T is None else T, cfg.d, cfg.E, cfg.k, cfg.n_shared, cfg.inter, cfg.prec)
+    dm = capi.dims(cfg.T if T is None else T, cfg.d, cfg.E, cfg.k, cfg.n_shared, cfg.inter, cfg.prec,
+                   cfg.route_groups, cfg.route_group_limit)
     return dm, torch.empty(capi.moe_workspace_size(dm), dtype=torch.uint8, device=DEV)
 
 
@@ -39,13 +40,20 @@ def test_bounded_wait_times_out_and_context_survives():
     assert float((x * 2).sum()) == 8.0                 # the context is still usable
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "mid"])
+ROUTE_CASES = {"tiny": {}, "ragged": {}, "mid": {},
+               # node-limited routing: experts on nodes, a token on at most `limit` of them
+               "ragged_nodes": dict(route_groups=5, route_group_limit=2),
+               "mid_nodes": dict(route_groups=8, route_group_limit=3)}
+
+
+@pytest.mark.parametrize("name", list(ROUTE_CASES))
 def test_route_parity(name):
-    cfg = synth.get_config(name)
+    cfg = synth.get_config(name.replace("_nodes", ""), **ROUTE_CASES[name])
     u, cent, bias = synth.tokens(cfg), synth.centroids(cfg), synth.bias(cfg)
     idx, gate, counts = _route_gpu(cfg, u, cent, bias)
-    r = oracle.route(synth.bf16_bits(u), synth.bf16_bits(cent), np.asarray(bias), cfg.k, want_all=True)
-    ties = check_selection(idx, r, np.asarray(bias), cfg.k)
+    r = oracle.route(synth.bf16_bits(u), synth.bf16_bits(cent), np.asarray(bias), cfg.k, want_all=True,
+                     groups=cfg.route_groups, group_limit=cfg.route_group_limit)
+    ties = check_selection(idx, r, np.asarray(bias), cfg.k, cfg.route_groups, cfg.route_group_limit)
     # counts are the histogram of the GPU's own selection, bit for bit
     np.testing.assert_array_equal(counts, np.bincount(idx.ravel(), minlength=cfg.E))
     if not ties:
@@ -139,8 +147,9 @@ def _forward_parity(cfg, sample=None, extra_chunks=True):
     bias = np.asarray(host.bias)
     res = gpu_layer_pass(layer, u.to(DEV), host.bias.to(DEV))
     ub = synth.bf16_bits(u)
-    r = oracle.route(ub, synth.bf16_bits(host.cent), bias, cfg.k, want_all=True)
-    check_routing_and_dispatch(res, r, bias, cfg.E, cfg.k)
+    r = oracle.route(ub, synth.bf16_bits(host.cent), bias, cfg.k, want_all=True, groups=cfg.route_groups,
+                     group_limit=cfg.route_group_limit)
+    check_routing_and_dispatch(res, r, bias, cfg.E, cfg.k, cfg.route_groups, cfg.route_group_limit)
     if sample is None:
         tokens = np.arange(cfg.T)
     else:
@@ -160,10 +169,10 @@ def test_forward_parity_full(name):
     assert err_y <= Y_TOL[cfg.prec]
 
 
-@pytest.mark.parametrize("name", ["mid", "mid_fp8"])
+@pytest.mark.parametrize("name", ["mid", "mid_fp8", "mid_nodes"])
 def test_forward_parity_mid_sampled(name):
-    base = synth.get_config("mid")
-    cfg = base if name == "mid" else synth.get_config("mid", prec="fp8")
+    extra = {"mid": {}, "mid_fp8": dict(prec="fp8"), "mid_nodes": dict(route_groups=8, route_group_limit=3)}
+    cfg = synth.get_config("mid", **extra[name])
     sample = np.arange(0, cfg.T, 29)           # 142 tokens from every part of the batch, plus chunk cover
     err, err_y = _forward_parity(cfg, sample)
     print(f"{name}: max|err|/rms h' = {err:.3e}, routed y = {err_y:.3e}")

@@ -454,3 +454,40 @@ def test_expert_rows_assemble_to_layer_output(name):
                          r["gate"][tokens])
     ref = oracle.layer_output(*args, fp8=fp8)
     np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12 * np.abs(ref).max())
+
+
+# ----------------------------------------------------------------------------
+# node-limited routing (ai.flicky.cc 2.1.2: a token goes to at most 4 nodes)
+@pytest.mark.parametrize("groups,limit,k", [(8, 2, 4), (8, 3, 6), (4, 1, 3), (10, 4, 8)])
+def test_node_limited_selection_matches_node_ranking_statement(groups, limit, k):
+    """The oracle's greedy selection under a node budget equals the statement
+    'keep the `limit` nodes with the best experts, then top-k inside them',
+    every token spans at most `limit` nodes, and the gates stay normalised
+    over the selected unbiased affinities."""
+    E = 40 if groups == 10 else 32
+    cfg = synth.get_config("ragged", E=E, k=k)
+    u, c = synth.tokens(cfg), synth.centroids(cfg)
+    b = np.asarray(synth.normal_f32(99, (E,), 0.03))
+    r = oracle.route(synth.bf16_bits(u), synth.bf16_bits(c), b, k, want_all=True, groups=groups, group_limit=limit)
+    score = r["s_all"] + b.astype(np.float64)
+    gs = E // groups
+    for t in range(cfg.T):
+        assert r["idx"][t].tolist() == brute.node_limited_topk(score[t], k, groups, limit)
+        assert len({int(e) // gs for e in r["idx"][t]}) <= limit
+    sel = np.take_along_axis(r["s_all"], r["idx"].astype(np.int64), 1)
+    np.testing.assert_allclose(r["gate"], sel / sel.sum(1, keepdims=True), rtol=0, atol=1e-12)
+    # the limit binds somewhere (else this test says nothing about it)
+    free = oracle.route(synth.bf16_bits(u), synth.bf16_bits(c), b, k)
+    assert (np.sort(free["idx"], 1) != np.sort(r["idx"], 1)).any()
+
+
+def test_node_limit_that_cannot_bind_changes_nothing():
+    """limit = groups, or a limit of at least k nodes: the plain top-k."""
+    cfg = synth.get_config("ragged")
+    u, c = synth.bf16_bits(synth.tokens(cfg)), synth.bf16_bits(synth.centroids(cfg))
+    b = np.asarray(synth.bias(cfg))
+    free = oracle.route(u, c, b, cfg.k)
+    for groups, limit in ((5, 5), (20, cfg.k), (10, cfg.k + 1)):
+        r = oracle.route(u, c, b, cfg.k, groups=groups, group_limit=limit)
+        np.testing.assert_array_equal(r["idx"], free["idx"])
+        np.testing.assert_array_equal(r["gate"], free["gate"])
