@@ -196,13 +196,26 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, const uint
  *   w13, w2   weights of the n_groups experts in the moe_weights layout
  *             (with their block scales for FP8).
  *   y         out [rows, d] bf16.
+ *   group_expert  NULL: group g uses the weights of expert g (the weight
+ *             arrays hold n_groups experts).  Otherwise [n_groups] int32
+ *             device array: group g uses the weights of expert
+ *             group_expert[g] < n_weight_experts, the number of experts the
+ *             weight arrays hold.  Several groups may share one expert's
+ *             weights: the copies of a replicated hot expert (ai.flicky.cc
+ *             3.5: popular experts are duplicated), or the rows an
+ *             expert-parallel rank receives for one expert from each sender
+ *             (ai.flicky.cc 3.4, EP with all-to-all).  An entry outside
+ *             [0, n_weight_experts) raises MOE_ERR_BAD_INDEX on the device and
+ *             uses expert 0.
+ * Limits: n_groups <= dims->E + dims->n_shared (the workspace's group tables
+ * are sized by dims), rows <= dims->T * dims->k.
  * The gate/up product and SiLU(g)*u are one fused tcgen05 GEMM; FP8 also
  * quantises h per 1 x 128 tile inside that GEMM before the down product.
  */
 moe_status moe_grouped_ffn(const moe_dims* dims, int32_t n_groups, int32_t rows, const int32_t* offsets,
-                           const void* x, const float* x_scale, const void* w13, const float* w13_scale,
-                           const void* w2, const float* w2_scale, uint16_t* y, void* ws,
-                           size_t ws_bytes, void* stream);
+                           const int32_t* group_expert, int32_t n_weight_experts, const void* x,
+                           const float* x_scale, const void* w13, const float* w13_scale, const void* w2,
+                           const float* w2_scale, uint16_t* y, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Combine (the layer equation of ai.flicky.cc 2.1.2):
@@ -237,6 +250,38 @@ moe_status moe_bias_update(int32_t E, int32_t T, int32_t k, const int32_t* count
  */
 moe_status moe_forward(const moe_dims* dims, const moe_weights* w, const uint16_t* u, const float* bias,
                        uint16_t* out, int32_t* counts_out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Redundant experts (ai.flicky.cc 3.5: popular experts are duplicated to even
+ * out the load).  A plan gives expert e replica_count[e] >= 1 copies, the
+ * physical slots replica_first[e] .. replica_first[e] + replica_count[e] - 1,
+ * and slot_expert[p] names the expert whose weights slot p uses; P = E +
+ * n_extra slots in all.  The copies share the expert's weights (nothing is
+ * duplicated in memory on one GPU; in an expert-parallel deployment each copy
+ * would live on another device).
+ *
+ * moe_plan_replicas: HOST function (all pointers host memory, no GPU work):
+ *   counts  [E] the experts' loads (e.g. the previous step's counts_out).
+ *   Each of the n_extra copies goes to the expert with the highest load per
+ *   copy, counts[e] / replica_count[e] (ties: lower index); then slots are
+ *   numbered expert by expert.  Outputs replica_first [E], replica_count [E],
+ *   slot_expert [E + n_extra].  Limits: 1 <= E <= 1024, 0 <= n_extra <= 1024.
+ *
+ * moe_forward_replicated: moe_forward with the plan (device copies of the
+ *   three tables; n_slots = P).  A token's pair (t, j) with expert e goes to
+ *   copy t mod replica_count[e]; the grouped GEMMs run one group per physical
+ *   slot on the shared weights.  h' is that of moe_forward; counts_out holds
+ *   the experts' (not the slots') loads.  The workspace must be at least
+ *   moe_workspace_size of dims with E replaced by n_slots (the per-expert
+ *   tables hold the slots).  A bad plan entry raises MOE_ERR_BAD_INDEX on the
+ *   device and the pair is left out.
+ */
+moe_status moe_plan_replicas(int32_t E, const int32_t* counts, int32_t n_extra, int32_t* replica_first,
+                             int32_t* replica_count, int32_t* slot_expert);
+moe_status moe_forward_replicated(const moe_dims* dims, const moe_weights* w, const uint16_t* u, const float* bias,
+                                  const int32_t* replica_first, const int32_t* replica_count,
+                                  const int32_t* slot_expert, int32_t n_slots, uint16_t* out, int32_t* counts_out,
+                                  void* ws, size_t ws_bytes, void* stream);
 
 /*
  * moe_forward with stage timing.  `events` holds n_events >= MOE_PROFILE_EVENTS

@@ -21,7 +21,8 @@ MOE_BF16, MOE_FP8_E4M3 = 0, 1
 # Every symbol include/moe.h declares.
 EXPORTS = (
     "moe_status_string", "moe_workspace_size", "moe_route", "moe_route_noalloc", "moe_permute", "moe_grouped_ffn",
-    "moe_combine", "moe_bias_update", "moe_forward", "moe_forward_profiled", "moe_pack_gate_up",
+    "moe_combine", "moe_bias_update", "moe_forward", "moe_forward_profiled", "moe_forward_replicated",
+    "moe_plan_replicas", "moe_pack_gate_up",
     "moe_quantize_fp8_blocks",
     "moe_read_device_status", "moe_selftest_wait_timeout",
 )
@@ -64,12 +65,15 @@ def lib() -> ctypes.CDLL:
             "moe_route": ([D, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
             "moe_route_noalloc": ([D, vp, vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
             "moe_permute": ([D, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
-            "moe_grouped_ffn": ([D, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
+            "moe_grouped_ffn": ([D, i32, i32, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
             "moe_combine": ([D, vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
             "moe_bias_update": ([i32, i32, i32, vp, f32, vp, vp], ctypes.c_int),
             "moe_forward": ([D, ctypes.POINTER(moe_weights), vp, vp, vp, vp, vp, sz, vp], ctypes.c_int),
             "moe_forward_profiled": ([D, ctypes.POINTER(moe_weights), vp, vp, vp, vp, vp, sz, vp,
                                       ctypes.POINTER(vp), i32], ctypes.c_int),
+            "moe_forward_replicated": ([D, ctypes.POINTER(moe_weights), vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp],
+                                       ctypes.c_int),
+            "moe_plan_replicas": ([i32, vp, i32, vp, vp, vp], ctypes.c_int),
             "moe_pack_gate_up": ([vp, vp, i32, i32, i32, vp, vp], ctypes.c_int),
             "moe_quantize_fp8_blocks": ([vp, i64, i32, vp, vp, vp], ctypes.c_int),
             "moe_read_device_status": ([vp, vp], ctypes.c_int),
@@ -146,10 +150,12 @@ def moe_permute(dm, topk_idx, u, offsets, perm, slot, x_perm, x_scale, ws, strea
                              _stream(stream)), "moe_permute")
 
 
-def moe_grouped_ffn(dm, n_groups, rows, offsets, x, x_scale, w13, w13_scale, w2, w2_scale, y, ws, stream=None):
-    _check(lib().moe_grouped_ffn(ctypes.byref(dm), int(n_groups), int(rows), _ptr(offsets), _ptr(x), _ptr(x_scale),
-                                 _ptr(w13), _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), _ptr(y), _ptr(ws),
-                                 ws.numel() * ws.element_size(), _stream(stream)), "moe_grouped_ffn")
+def moe_grouped_ffn(dm, n_groups, rows, offsets, x, x_scale, w13, w13_scale, w2, w2_scale, y, ws, stream=None,
+                    group_expert=None, n_weight_experts=0):
+    _check(lib().moe_grouped_ffn(ctypes.byref(dm), int(n_groups), int(rows), _ptr(offsets), _ptr(group_expert),
+                                 int(n_weight_experts), _ptr(x), _ptr(x_scale), _ptr(w13), _ptr(w13_scale), _ptr(w2),
+                                 _ptr(w2_scale), _ptr(y), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_grouped_ffn")
 
 
 def moe_combine(dm, u, shared_y, y_perm, slot, topk_gate, out, stream=None):
@@ -171,6 +177,28 @@ def moe_forward(dm, weights: moe_weights, u, bias, out, counts_out, ws, stream=N
     _check(lib().moe_forward(ctypes.byref(dm), ctypes.byref(weights), _ptr(u), _ptr(bias), _ptr(out),
                              _ptr(counts_out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "moe_forward")
+
+
+def moe_plan_replicas(counts, n_extra):
+    """Host plan of n_extra copies of the most loaded experts: (replica_first,
+    replica_count, slot_expert) as int32 CPU tensors (counts: CPU int32 [E])."""
+    counts = counts.to(torch.int32).contiguous()
+    assert not counts.is_cuda
+    E = counts.numel()
+    first = torch.empty(E, dtype=torch.int32)
+    copies = torch.empty(E, dtype=torch.int32)
+    slot_expert = torch.empty(E + int(n_extra), dtype=torch.int32)
+    _check(lib().moe_plan_replicas(int(E), _ptr(counts), int(n_extra), _ptr(first), _ptr(copies), _ptr(slot_expert)),
+           "moe_plan_replicas")
+    return first, copies, slot_expert
+
+
+def moe_forward_replicated(dm, weights: moe_weights, u, bias, replica_first, replica_count, slot_expert, out,
+                           counts_out, ws, stream=None):
+    _check(lib().moe_forward_replicated(ctypes.byref(dm), ctypes.byref(weights), _ptr(u), _ptr(bias),
+                                        _ptr(replica_first), _ptr(replica_count), _ptr(slot_expert),
+                                        int(slot_expert.numel()), _ptr(out), _ptr(counts_out), _ptr(ws),
+                                        ws.numel() * ws.element_size(), _stream(stream)), "moe_forward_replicated")
 
 
 PROFILE_STAGES = ("router_gemm", "topk", "scan_plan", "gather", "routed_gate_up", "routed_down",

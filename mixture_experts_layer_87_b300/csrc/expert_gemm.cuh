@@ -158,10 +158,12 @@ __device__ __forceinline__ int xitems(const XGemmArgs& a, int nb) {
   return __ldg(a.ch_total) * nb;
 }
 
-// Item `tile` -> (group, weight block, chunk).  Items are ordered group by
-// group, and inside a group weight block by weight block with the chunks
-// fastest, so group g owns items [mt_start_g * nb, (mt_start_g + nch_g) * nb)
-// and chunk_group[tile / nb] is its group: two dependent loads per item.
+// Item `tile` -> (expert weights, weight block, chunk).  Items are ordered
+// group by group, and inside a group weight block by weight block with the
+// chunks fastest, so group g owns items [mt_start_g * nb, (mt_start_g +
+// nch_g) * nb) and chunk_group[tile / nb] names its group (low 16 bits) and
+// the expert whose weights the group uses (high 16 bits; plan_kernel fills
+// both): two dependent loads per item.
 __device__ __forceinline__ bool xdecode(const XGemmArgs& a, int tile, int items, int nb, XTile& t) {
   constexpr int ch = kXChunk;
   if (tile >= items) return false;
@@ -177,11 +179,11 @@ __device__ __forceinline__ bool xdecode(const XGemmArgs& a, int tile, int items,
     t.n_valid = min(ch, a.uni_m - t.c * ch);
     return true;
   }
-  const int g = __ldg(a.chunk_group + tile / nb);
-  const int4 G = __ldg(reinterpret_cast<const int4*>(a.groups) + g);  // {a_row0, out_row0, m, mt_start}
+  const int cg = __ldg(a.chunk_group + tile / nb);
+  const int4 G = __ldg(reinterpret_cast<const int4*>(a.groups) + (cg & 0xFFFF));  // {a_row0, out_row0, m, mt_start}
   const int nch = (G.z + ch - 1) / ch;
   const int local = tile - G.w * nb;
-  t.g = g;
+  t.g = cg >> 16;  // the weights' expert
   t.fb = local / nch;
   t.c = local - t.fb * nch;
   t.a_row = G.x + t.c * ch;

@@ -142,11 +142,11 @@ __device__ __forceinline__ bool f8decode(const GemmArgs& a, int tile, int items,
     tc.rows_valid = min(BM, a.uni_m - tc.m_idx * BM);
     return true;
   }
-  const int g = __ldg(a.chunk_group + tile / nb);
-  const int4 G = __ldg(reinterpret_cast<const int4*>(a.groups) + g);  // {a_row0, out_row0, m, mt_start}
+  const int cg = __ldg(a.chunk_group + tile / nb);  // group | the weights' expert << 16
+  const int4 G = __ldg(reinterpret_cast<const int4*>(a.groups) + (cg & 0xFFFF));  // {a_row0, out_row0, m, mt_start}
   const int mt = (G.z + BM - 1) / BM;
   const int local = tile - G.w * nb;
-  tc.g = g;
+  tc.g = cg >> 16;
   tc.n_idx = local / mt;
   tc.m_idx = local - tc.n_idx * mt;
   tc.a_row = G.x + tc.m_idx * BM;

@@ -205,12 +205,17 @@ __global__ void __launch_bounds__(256) expert_scan_kernel(const uint32_t* __rest
 // offs_in != nullptr the counts come from untrusted offsets
 // (moe_grouped_ffn): they are made non-decreasing and clipped to
 // [0, clamp_rows], flagging any repair.
-// chunk_group (optional, cg_cap entries) receives the group of every chunk,
-// so a GEMM maps a chunk index to its group with one load.
+// chunk_group (optional, cg_cap entries) receives, for every chunk, its group
+// g in the low 16 bits and the expert whose weights the group uses in the
+// high 16 bits -- group_weight[g] (checked against n_weights: an entry
+// outside [0, n_weights) is flagged and replaced by 0), or g when group_weight
+// is nullptr -- so a GEMM maps a chunk index to both with one load.  G <= 65535.
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ cnt, const int32_t* __restrict__ offs_in,
                                                     int G, int clamp_rows, int chunk, int32_t* __restrict__ offsets_out,
                                                     GroupEntry* __restrict__ groups, int32_t* __restrict__ mt_total,
-                                                    int32_t* __restrict__ chunk_group, int cg_cap, int* status) {
+                                                    int32_t* __restrict__ chunk_group, int cg_cap,
+                                                    const int32_t* __restrict__ group_weight, int n_weights,
+                                                    int* status) {
   __shared__ int warp_sums[32];
   __shared__ int carry_rows, carry_mt;
   if (threadIdx.x == 0) {
@@ -240,8 +245,17 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
       const int off = offs_in ? a0 : carry_rows + ex_rows;
       if (offsets_out) offsets_out[g] = off;
       groups[g] = GroupEntry{off, off, rows, carry_mt + ex_mt};
-      if (chunk_group)
-        for (int j = carry_mt + ex_mt; j < carry_mt + ex_mt + mt && j < cg_cap; ++j) chunk_group[j] = g;
+      if (chunk_group) {
+        int w = g;
+        if (group_weight) {
+          w = group_weight[g];
+          if (w < 0 || w >= n_weights || w > 0xFFFF) {
+            record_status(status, ST_BAD_INDEX);
+            w = 0;
+          }
+        }
+        for (int j = carry_mt + ex_mt; j < carry_mt + ex_mt + mt && j < cg_cap; ++j) chunk_group[j] = g | (w << 16);
+      }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -476,6 +490,36 @@ __global__ void pack_gate_up_kernel(const uint4* __restrict__ w1, const uint4* _
     const int64_t srow = e * I + 128 * j + (within & 127);
     w13[i] = src[srow * nc + c];
   }
+}
+
+// ---------------------------------------------------------------------------
+// Redundant experts (ai.flicky.cc 3.5: popular experts are duplicated to even
+// out the load).  Expert e has replica_count[e] copies, the physical slots
+// replica_first[e] ...; the pair (t, j) goes to copy t mod replica_count[e]:
+// idx[t, j] is rewritten in place from the expert to its physical slot and the
+// token's bit is set in the slot's row of the dispatch mask.  A bad expert
+// index or plan entry is flagged and the pair left out.
+__global__ void assign_replicas_kernel(int32_t* __restrict__ idx, int64_t n, int k, int E,
+                                       const int32_t* __restrict__ replica_first,
+                                       const int32_t* __restrict__ replica_count, int P, uint32_t* __restrict__ mask,
+                                       int W, int* status) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int e = idx[i];
+  const int64_t t = i / k;
+  if (e < 0 || e >= E) {
+    record_status(status, ST_BAD_INDEX);
+    return;
+  }
+  const int first = replica_first[e], copies = replica_count[e];
+  const int p = copies > 0 ? first + static_cast<int>(t % copies) : -1;
+  if (copies <= 0 || first < 0 || p >= P) {
+    record_status(status, ST_BAD_INDEX);
+    idx[i] = -1;  // dispatch skips it (and flags it again)
+    return;
+  }
+  idx[i] = p;
+  atomicOr(&mask[(int64_t)p * W + (t >> 5)], 1u << (t & 31));
 }
 
 // Self-test: one warp waits on an mbarrier nothing arrives on; the bounded

@@ -244,12 +244,13 @@ moe_status enqueue_route(const moe_dims& d, const uint16_t* u, const uint16_t* c
 moe_status enqueue_dispatch(const moe_dims& d, const int32_t* idx, const uint16_t* u, const uint32_t* mask,
                             int32_t* wprefix, int32_t* cnt, int32_t* offsets, GroupEntry* groups, int32_t* mt_total,
                             int32_t* cgroup, int32_t* perm, int32_t* slot, void* x, float* xs, uint8_t* uq, float* uqs, int* status,
-                            cudaStream_t st, Recorder* rec = nullptr) {
+                            cudaStream_t st, Recorder* rec = nullptr, const int32_t* group_weight = nullptr,
+                            int n_weights = 0) {
   const int W = (d.T + 31) / 32;
   expert_scan_kernel<<<d.E, 256, 0, st>>>(mask, W, wprefix, cnt);
   MOE_TRY(launched());
   plan_kernel<<<1, 1024, 0, st>>>(cnt, nullptr, d.E, 0, chunk_rows(d), offsets, groups, mt_total, cgroup,
-                                  static_cast<int>(cgroup_cap(d)), status);
+                                  static_cast<int>(cgroup_cap(d)), group_weight, n_weights, status);
   MOE_TRY(launched());
   if (rec) MOE_TRY(rec->mark());
   if (d.T == 0) return rec ? rec->mark() : MOE_OK;  // the offsets (all zero) are the whole result
@@ -343,7 +344,12 @@ struct FfnOperands {
   float* hs;
   uint16_t* y;
   int64_t rows_cap;  // rows allocated in h and y
+  const int32_t* group_weight = nullptr;  // table groups -> experts of the weight arrays (nullptr: g -> g)
+  int32_t n_weights = 0;                  // experts in the weight arrays when group_weight is given
 };
+
+// Experts held in the weight arrays of a launch over n_groups groups.
+int64_t weight_experts(const FfnOperands& o, int n_groups) { return o.group_weight ? o.n_weights : n_groups; }
 
 // FP8: tokens on the 128 TMEM lanes (128-row tiles of grouped_gemm_kernel),
 // so the promotion scale of a lane is one activation scale per k-block.
@@ -353,9 +359,9 @@ moe_status enqueue_ffn_fp8(const moe_dims& d, const FfnOperands& o, int n_groups
   const int I = d.inter, D = d.d;
   CUtensorMap ta1, tb1, ta2, tb2;
   MOE_TRY(make_tmap(&ta1, o.x, true, o.x_rows, D, 128));
-  MOE_TRY(make_tmap(&tb1, o.w13, true, int64_t(n_groups) * 2 * I, D, 256));
+  MOE_TRY(make_tmap(&tb1, o.w13, true, weight_experts(o, n_groups) * 2 * I, D, 256));
   MOE_TRY(make_tmap(&ta2, o.h, true, o.rows_cap, I, 128));
-  MOE_TRY(make_tmap(&tb2, o.w2, true, int64_t(n_groups) * D, I, 256));
+  MOE_TRY(make_tmap(&tb2, o.w2, true, weight_experts(o, n_groups) * D, I, 256));
   const int64_t mt = table ? cdiv(o.rows_cap + 127 * int64_t(n_groups), 128) : int64_t(n_groups) * cdiv(uni_m, 128);
 
   GemmArgs a = base_args(status);
@@ -410,9 +416,9 @@ moe_status enqueue_ffn(const moe_dims& d, const FfnOperands& o, int n_groups, co
   constexpr int CH = kChunkBf16;
   CUtensorMap tx1, tw1, tx2, tw2;
   MOE_TRY(make_tmap(&tx1, o.x, false, o.x_rows, D, CH));
-  MOE_TRY(make_tmap(&tw1, o.w13, false, int64_t(n_groups) * 2 * I, D, 256));
+  MOE_TRY(make_tmap(&tw1, o.w13, false, weight_experts(o, n_groups) * 2 * I, D, 256));
   MOE_TRY(make_tmap(&tx2, o.h, false, o.rows_cap, I, CH));
-  MOE_TRY(make_tmap(&tw2, o.w2, false, int64_t(n_groups) * D, I, 256));
+  MOE_TRY(make_tmap(&tw2, o.w2, false, weight_experts(o, n_groups) * D, I, 256));
   // upper bound of the token chunks: every group adds at most one partial chunk
   const int64_t chunks = table ? cdiv(o.rows_cap + int64_t(CH - 1) * n_groups, CH)
                                : int64_t(n_groups) * cdiv(uni_m, CH);
@@ -529,13 +535,14 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, const uint
 }
 
 moe_status moe_grouped_ffn(const moe_dims* dims, int32_t n_groups, int32_t rows, const int32_t* offsets,
-                           const void* x, const float* x_scale, const void* w13, const float* w13_scale,
-                           const void* w2, const float* w2_scale, uint16_t* y, void* ws, size_t ws_bytes,
-                           void* stream) {
+                           const int32_t* group_expert, int32_t n_weight_experts, const void* x,
+                           const float* x_scale, const void* w13, const float* w13_scale, const void* w2,
+                           const float* w2_scale, uint16_t* y, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(check_dims(dims));
   MOE_TRY(check_ws(dims, ws, ws_bytes));
   const bool fp8 = dims->prec == MOE_FP8_E4M3;
   if (n_groups <= 0 || n_groups > dims->E + dims->n_shared || rows < 0) return MOE_ERR_INVALID_ARG;
+  if (group_expert && n_weight_experts <= 0) return MOE_ERR_INVALID_ARG;
   if (int64_t(rows) > int64_t(dims->T) * dims->k) return MOE_ERR_WORKSPACE;
   if (!offsets || !x || !w13 || !w2 || !y) return MOE_ERR_INVALID_ARG;
   if (fp8 && (!x_scale || !w13_scale || !w2_scale)) return MOE_ERR_INVALID_ARG;
@@ -551,10 +558,10 @@ moe_status moe_grouped_ffn(const moe_dims* dims, int32_t n_groups, int32_t rows,
   int* queue = at<int>(ws, L.queue);
   MOE_TRY(cuda_ok(cudaMemsetAsync(queue, 0, 2 * sizeof(int), st)));
   plan_kernel<<<1, 1024, 0, st>>>(nullptr, offsets, n_groups, rows, chunk_rows(*dims), nullptr, groups, mt_total,
-                                  cgroup, static_cast<int>(cgroup_cap(*dims)), status);
+                                  cgroup, static_cast<int>(cgroup_cap(*dims)), group_expert, n_weight_experts, status);
   MOE_TRY(launched());
   FfnOperands o{x, x_scale, rows, w13, w13_scale, w2, w2_scale, at<void>(ws, L.h),
-                fp8 ? at<float>(ws, L.hs) : nullptr, y, rows};
+                fp8 ? at<float>(ws, L.hs) : nullptr, y, rows, group_expert, n_weight_experts};
   return enqueue_ffn(*dims, o, n_groups, groups, mt_total, cgroup, 0, queue, status, st);
 }
 
@@ -586,18 +593,39 @@ moe_status moe_forward(const moe_dims* dims, const moe_weights* w, const uint16_
   return moe_forward_profiled(dims, w, u, bias, out, counts_out, ws, ws_bytes, stream, nullptr, 0);
 }
 
-moe_status moe_forward_profiled(const moe_dims* dims, const moe_weights* w, const uint16_t* u, const float* bias,
-                                uint16_t* out, int32_t* counts_out, void* ws, size_t ws_bytes, void* stream,
-                                void* const* events, int32_t n_events) {
+}  // extern "C"
+
+namespace {
+
+// Copies of hot experts (moe_forward_replicated): device tables of the plan.
+struct ReplicaPlan {
+  const int32_t* first;        // [E]
+  const int32_t* count;        // [E]
+  const int32_t* slot_expert;  // [P]
+  int32_t P;                   // physical slots
+};
+
+// The dims the workspace of a forward is laid out for: with a replica plan
+// the per-expert tables hold the P physical slots.
+moe_dims ws_dims(const moe_dims& d, const ReplicaPlan* rp) {
+  moe_dims w = d;
+  if (rp && rp->P > w.E) w.E = rp->P;
+  return w;
+}
+
+moe_status forward_impl(const moe_dims* dims, const moe_weights* w, const uint16_t* u, const float* bias,
+                        uint16_t* out, int32_t* counts_out, void* ws, size_t ws_bytes, void* stream,
+                        void* const* events, int32_t n_events, const ReplicaPlan* rp) {
   MOE_TRY(check_dims(dims));
-  MOE_TRY(check_ws(dims, ws, ws_bytes));
+  const moe_dims wd = ws_dims(*dims, rp);
+  MOE_TRY(check_ws(&wd, ws, ws_bytes));
   MOE_TRY(check_weights(*dims, w));
   // u and out may be empty (null) when T == 0
   if (!bias || (d_T_nonzero(dims) && (!u || !out)) || !aligned16(u) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
   if (events && n_events < MOE_PROFILE_EVENTS) return MOE_ERR_INVALID_ARG;
   const moe_dims& d = *dims;
   const bool fp8 = d.prec == MOE_FP8_E4M3;
-  const Layout L = make_layout(d);
+  const Layout L = make_layout(wd);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Recorder recorder;
   recorder.ev = events;
@@ -612,27 +640,38 @@ moe_status moe_forward_profiled(const moe_dims* dims, const moe_weights* w, cons
   if (d.T == 0) return cuda_ok(cudaMemsetAsync(counts, 0, sizeof(int32_t) * d.E, st));
   const int W = (d.T + 31) / 32;
   uint32_t* mask = at<uint32_t>(ws, L.mask);
-  MOE_TRY(cuda_ok(cudaMemsetAsync(mask, 0, sizeof(uint32_t) * size_t(d.E) * W, st)));
+  MOE_TRY(cuda_ok(cudaMemsetAsync(mask, 0, sizeof(uint32_t) * size_t(wd.E) * W, st)));
 
   int32_t* idx = at<int32_t>(ws, L.idx);
   float* gate = at<float>(ws, L.gate);
-  MOE_TRY(enqueue_route(d, u, w->centroids, bias, idx, gate, counts, mask, at<float>(ws, L.z), status, st, rec));
+  // with copies of hot experts the dispatch mask is over physical slots, set
+  // by the replica assignment instead of the router
+  MOE_TRY(enqueue_route(d, u, w->centroids, bias, idx, gate, counts, rp ? nullptr : mask, at<float>(ws, L.z), status,
+                        st, rec));
+  const int64_t R = int64_t(d.T) * d.k;
+  moe_dims dd = d;  // the dispatch's view: one group per physical slot
+  if (rp) {
+    assign_replicas_kernel<<<static_cast<unsigned>(cdiv(R, 256)), 256, 0, st>>>(idx, R, d.k, d.E, rp->first, rp->count,
+                                                                                rp->P, mask, W, status);
+    MOE_TRY(launched());
+    dd.E = rp->P;
+  }
 
   GroupEntry* groups = at<GroupEntry>(ws, L.groups);
   int32_t* mt_total = at<int32_t>(ws, L.mt_total);
   int32_t* slot = at<int32_t>(ws, L.slot);
-  const int64_t R = int64_t(d.T) * d.k;
-  MOE_TRY(enqueue_dispatch(d, idx, u, mask, at<int32_t>(ws, L.wprefix), at<int32_t>(ws, L.cnt),
+  MOE_TRY(enqueue_dispatch(dd, idx, u, mask, at<int32_t>(ws, L.wprefix), at<int32_t>(ws, L.cnt),
                            at<int32_t>(ws, L.offsets), groups, mt_total, at<int32_t>(ws, L.cgroup),
                            at<int32_t>(ws, L.perm), slot,
                            at<void>(ws, L.x), fp8 ? at<float>(ws, L.xs) : nullptr,
                            fp8 ? at<uint8_t>(ws, L.uq) : nullptr, fp8 ? at<float>(ws, L.uqs) : nullptr, status, st,
-                           rec));
+                           rec, rp ? rp->slot_expert : nullptr, d.E));
 
   // routed experts: groups from the device table
   FfnOperands ro{at<void>(ws, L.x), fp8 ? at<float>(ws, L.xs) : nullptr, R, w->w13, w->w13_scale, w->w2,
-                 w->w2_scale, at<void>(ws, L.h), fp8 ? at<float>(ws, L.hs) : nullptr, at<uint16_t>(ws, L.y), R};
-  MOE_TRY(enqueue_ffn(d, ro, d.E, groups, mt_total, at<int32_t>(ws, L.cgroup), 0, queue, status, st, rec));
+                 w->w2_scale, at<void>(ws, L.h), fp8 ? at<float>(ws, L.hs) : nullptr, at<uint16_t>(ws, L.y), R,
+                 rp ? rp->slot_expert : nullptr, d.E};
+  MOE_TRY(enqueue_ffn(d, ro, dd.E, groups, mt_total, at<int32_t>(ws, L.cgroup), 0, queue, status, st, rec));
 
   // shared experts: every token, n_shared uniform groups
   uint16_t* ysh = at<uint16_t>(ws, L.ysh);
@@ -651,6 +690,53 @@ moe_status moe_forward_profiled(const moe_dims* dims, const moe_weights* w, cons
       at<const __nv_bfloat16>(ws, L.y), slot, gate, d.T, d.d, d.k, R, reinterpret_cast<__nv_bfloat16*>(out), status);
   MOE_TRY(launched());
   return rec ? rec->mark() : MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_forward_profiled(const moe_dims* dims, const moe_weights* w, const uint16_t* u, const float* bias,
+                                uint16_t* out, int32_t* counts_out, void* ws, size_t ws_bytes, void* stream,
+                                void* const* events, int32_t n_events) {
+  return forward_impl(dims, w, u, bias, out, counts_out, ws, ws_bytes, stream, events, n_events, nullptr);
+}
+
+moe_status moe_plan_replicas(int32_t E, const int32_t* counts, int32_t n_extra, int32_t* replica_first,
+                             int32_t* replica_count, int32_t* slot_expert) {
+  if (E <= 0 || E > 1024 || n_extra < 0 || n_extra > 1024 || !counts || !replica_first || !replica_count ||
+      (!slot_expert && E + n_extra > 0))
+    return MOE_ERR_INVALID_ARG;
+  for (int e = 0; e < E; ++e) {
+    if (counts[e] < 0) return MOE_ERR_INVALID_ARG;
+    replica_count[e] = 1;
+  }
+  // each extra copy goes to the expert with the highest load per copy
+  // (counts[e] / copies[e], compared exactly as counts[a] * copies[b] vs
+  // counts[b] * copies[a]; ties to the lower index)
+  for (int r = 0; r < n_extra; ++r) {
+    int best = 0;
+    for (int e = 1; e < E; ++e)
+      if (int64_t(counts[e]) * replica_count[best] > int64_t(counts[best]) * replica_count[e]) best = e;
+    ++replica_count[best];
+  }
+  int32_t p = 0;
+  for (int e = 0; e < E; ++e) {
+    replica_first[e] = p;
+    for (int c = 0; c < replica_count[e]; ++c) slot_expert[p++] = e;
+  }
+  return MOE_OK;
+}
+
+moe_status moe_forward_replicated(const moe_dims* dims, const moe_weights* w, const uint16_t* u, const float* bias,
+                                  const int32_t* replica_first, const int32_t* replica_count,
+                                  const int32_t* slot_expert, int32_t n_slots, uint16_t* out, int32_t* counts_out,
+                                  void* ws, size_t ws_bytes, void* stream) {
+  MOE_TRY(check_dims(dims));
+  if (!replica_first || !replica_count || !slot_expert || n_slots < dims->E || n_slots > 2048)
+    return MOE_ERR_INVALID_ARG;
+  const ReplicaPlan rp{replica_first, replica_count, slot_expert, n_slots};
+  return forward_impl(dims, w, u, bias, out, counts_out, ws, ws_bytes, stream, nullptr, 0, &rp);
 }
 
 moe_status moe_pack_gate_up(const uint16_t* w1, const uint16_t* w3, int32_t E, int32_t inter, int32_t d,

@@ -147,3 +147,33 @@ class HostPipeline:
                 self.copied_out[b].record(self.s_out)
             self.used[b] = True
         start.wait_stream(self.s_out)
+
+
+class ReplicatedExperts:
+    """Copies of the most loaded experts of a layer (moe_plan_replicas), run
+    by moe_forward_replicated: the copies share the layer's weights, and the
+    plan tables live on the device with a workspace sized for the slots."""
+
+    def __init__(self, layer: MoELayer, counts: torch.Tensor, n_extra: int):
+        first, copies, slot_expert = capi.moe_plan_replicas(counts.detach().cpu(), n_extra)
+        self.layer = layer
+        self.replica_count_host = copies
+        self.slot_expert_host = slot_expert
+        dev = layer.device
+        self.replica_first = first.to(dev)
+        self.replica_count = copies.to(dev)
+        self.slot_expert = slot_expert.to(dev)
+        wd = capi.dims(layer.T, layer.d, layer.E + n_extra, layer.k, layer.n_shared, layer.inter, layer.prec)
+        self.ws = torch.empty(capi.moe_workspace_size(wd), dtype=torch.uint8, device=dev)
+
+    def forward(self, u: torch.Tensor, bias: torch.Tensor, out: torch.Tensor | None = None,
+                counts: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        L = self.layer
+        if out is None:
+            out = torch.empty((L.T, L.d), dtype=torch.bfloat16, device=L.device)
+        capi.moe_forward_replicated(L.dims, L.weights(), u, bias, self.replica_first, self.replica_count,
+                                    self.slot_expert, out, counts, self.ws, stream)
+        return out
+
+    def status(self) -> int:
+        return capi.moe_read_device_status(self.ws)

@@ -92,8 +92,11 @@ def test_calls_reject_null_and_small_workspace_without_a_gpu(lib):
     n8 = capi.moe_workspace_size(d8)
     assert lib.moe_permute(ctypes.byref(d8), fake, fake, fake, fake, fake, fake, None, fake, n8, None) == 1
     # grouped ffn: more rows than the workspace was sized for
-    assert lib.moe_grouped_ffn(ctypes.byref(dm), 2, 64 * 4 + 1, fake, fake, None, fake, None, fake, None, fake,
-                               fake, need, None) == 3
+    assert lib.moe_grouped_ffn(ctypes.byref(dm), 2, 64 * 4 + 1, fake, None, 0, fake, None, fake, None, fake, None,
+                               fake, fake, need, None) == 3
+    # grouped ffn: a group -> expert table without the number of experts it indexes
+    assert lib.moe_grouped_ffn(ctypes.byref(dm), 2, 64, fake, fake, 0, fake, None, fake, None, fake, None,
+                               fake, fake, need, None) == 1
     # bias update: k > E
     assert lib.moe_bias_update(4, 10, 5, fake, ctypes.c_float(0.001), fake, None) == 1
     # block quantiser: shape not a multiple of 128
