@@ -56,7 +56,9 @@ typedef enum {
                                was compiled to another register count than its warpgroup register
                                split assumes (a build problem: nothing is launched) */
   MOE_ERR_TIMEOUT = 5,      /* device: a bounded wait inside a kernel ran out */
-  MOE_ERR_BAD_INDEX = 6     /* device: an expert index outside [0, E) */
+  MOE_ERR_BAD_INDEX = 6,    /* device: an expert index outside [0, E) */
+  MOE_ERR_OUT_OF_RANGE = 7  /* device, range-checked build only (-DMOE_CHECK): a computed index outside
+                               its buffer; the access was skipped */
 } moe_status;
 
 typedef enum { MOE_BF16 = 0, MOE_FP8_E4M3 = 1 } moe_precision;

@@ -14,7 +14,9 @@ import os
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libmoe_b300.so")
+# MOE_B300_LIBRARY=check loads the range-checked build (build.py --check)
+LIB_PATH = os.path.join(_PKG, "libmoe_b300_check.so" if os.environ.get("MOE_B300_LIBRARY") == "check"
+                        else "libmoe_b300.so")
 
 MOE_BF16, MOE_FP8_E4M3 = 0, 1
 

@@ -54,6 +54,10 @@ struct XGemmArgs {
   int64_t out_ld;
   int* queue;           // item counter, zero at launch
   int* status;
+#ifdef MOE_CHECK
+  int64_t w_rows;       // rows of the weight tensor (range-checked build only)
+  int32_t out_rows;     // rows allocated in out (range-checked build only)
+#endif
 };
 
 // ---------------------------------------------------------------------------
@@ -269,6 +273,10 @@ __global__ void __launch_bounds__(kXThreads, 1)
         int v[6];
         if (!ring_take(ring, lt, v, args.status, abort_flag, false) || v[0] < 0) break;
         const int w_row = v[0] * args.Nw + v[1] * 256, a_row = v[3];
+        // TMA fills rows past a tensor's end with zeros; a tile that starts
+        // outside its tensor is still a wrong coordinate
+        (void)MOE_IN_RANGE(args.status, w_row, args.w_rows);
+        (void)MOE_IN_RANGE(args.status, a_row, args.x_rows);
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb, ++it) {
           const uint32_t s = it % STAGES;
@@ -346,7 +354,10 @@ __global__ void __launch_bounds__(kXThreads, 1)
       if (v[0] < 0) break;
       const int fb = v[1], out_row = v[4], n_valid = v[5];
       const int tok_lo = hg * TOK;
-      const int tok_n = max(0, min(TOK, n_valid - tok_lo));  // valid tokens of my half
+      // the item's output rows lie inside out (range-checked build; else skipped)
+      const bool rows_ok = MOE_IN_RANGE(args.status, out_row, args.out_rows) &&
+                           MOE_IN_RANGE(args.status, out_row + max(n_valid, 1) - 1, args.out_rows);
+      const int tok_n = rows_ok ? max(0, min(TOK, n_valid - tok_lo)) : 0;  // valid tokens of my half
       const uint32_t b = lt % NACC, u = lt / NACC;
       ok = __all_sync(0xffffffffu, xwait(&acc_full[b], u & 1, args.status, abort_flag));
       if (!ok) break;

@@ -275,7 +275,8 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
           if (lane < 2 * AHEAD) {
             const int j = lane & 1, kb = lane >> 1;
             const int blk_row = (tc.g * args.b_rows_per_group + tc.n_idx * BN) / 128 + j;
-            const bool blk_in = EPI == Epi::SWIGLU || tc.n_idx * BN + j * 128 < args.N;
+            const bool blk_in = (EPI == Epi::SWIGLU || tc.n_idx * BN + j * 128 < args.N) &&
+                                MOE_IN_RANGE(args.status, blk_row, args.b_rows / 128);
             ss[AHEAD * 128 + kb * 2 + j] =
                 kb < num_kb && blk_in ? __ldg(args.b_scale + (int64_t)blk_row * KB + kb) : 0.0f;
           }
@@ -300,6 +301,8 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
           int v[6];
           if (!ring_take(ring, lt, v, args.status, abort_flag, false) || v[0] < 0) break;
           const int b_row = v[0] * args.b_rows_per_group + v[2] * BN, a_row = v[3];
+          (void)MOE_IN_RANGE(args.status, b_row, args.b_rows);  // a tile starting outside its tensor
+          (void)MOE_IN_RANGE(args.status, a_row, args.a_rows_cap);
           bool ok = true;
           for (int kb = 0; kb < num_kb; ++kb, ++it) {
             const uint32_t s = it % STAGES;
@@ -405,10 +408,15 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
       const bool warp_rows = quarter * 32 < tc.rows_valid;
       const int a_row = tc.a_row + r;
       const bool a_in = a_row < args.a_rows_cap;
-      const float* sa_ptr = args.a_scale + a_row;
       const int b_row = tc.g * args.b_rows_per_group + tc.n_idx * BN;
+      // range-checked build: the scale rows read and the output rows written
+      // lie inside their tensors (else skipped)
+      const bool blk_ok = (EPI == Epi::SWIGLU || tc.n_idx * BN + blk * 128 < args.N) &&
+                          MOE_IN_RANGE(args.status, b_row / 128 + (EPI == Epi::SWIGLU ? 1 : blk), args.b_rows / 128);
+      const bool out_ok = MOE_IN_RANGE(args.status, tc.out_row, args.out_rows) &&
+                          MOE_IN_RANGE(args.status, tc.out_row + max(tc.rows_valid, 1) - 1, args.out_rows);
+      const float* sa_ptr = args.a_scale + a_row;
       const float* sb_ptr = args.b_scale + (int64_t)(b_row / 128) * KB;
-      const bool blk_ok = EPI == Epi::SWIGLU || tc.n_idx * BN + blk * 128 < args.N;
       const float* sb0_ptr = sb_ptr + (int64_t)blk * KB;                          // gate / my block
       const float* sb1_ptr = sb_ptr + (EPI == Epi::SWIGLU ? KB : (int64_t)blk * KB);  // up / my block
       uint64_t acc2[NCH * 8];  // acc2[c] = columns (2c, 2c + 1) of my NCH * 16
@@ -491,7 +499,7 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
         // h is a GEMM output known to fp32 accuracy: its codes are taken from
         // h * (1/scale), one correctly rounded reciprocal per row
         const float inv = 1.0f / scale;
-        if (row_ok) {
+        if (row_ok && out_ok) {
           uint8_t* q = static_cast<uint8_t*>(args.out) + (int64_t)(tc.out_row + r) * args.out_ld + tc.n_idx * 128 +
                        cg * NP * 16;
 #pragma unroll
@@ -510,7 +518,7 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
           if (cg == 0) args.out_scale[(int64_t)tc.n_idx * args.out_scale_ld + tc.out_row + r] = scale;
         }
       } else if constexpr (S::template stage_out<EPI>()) {
-        if (warp_rows && blk_ok) {
+        if (warp_rows && blk_ok && out_ok) {
           uint8_t* ycol = static_cast<uint8_t*>(args.out) + (int64_t)(tc.n_idx * BN + cg * NCH * 16) * 2;
 #pragma unroll
           for (int c = 0; c < NCH / 2; ++c) {
@@ -526,7 +534,7 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
           }
         }
       } else {
-        if (row_ok && blk_ok) {
+        if (row_ok && blk_ok && out_ok) {
           __nv_bfloat16* o = static_cast<__nv_bfloat16*>(args.out) + (int64_t)(tc.out_row + r) * args.out_ld +
                              tc.n_idx * BN + cg * NCH * 16;
 #pragma unroll

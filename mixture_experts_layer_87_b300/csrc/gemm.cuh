@@ -51,6 +51,12 @@ struct GemmArgs {
   int64_t out_scale_ld;
   int* queue;                // item counter, zero at launch
   int* status;
+#ifdef MOE_CHECK
+  // extents the range-checked build checks against (absent from the normal
+  // build: a larger argument block costs the 16-warp epilogue a register spill)
+  int64_t b_rows;            // rows of B
+  int32_t out_rows;          // rows allocated in out
+#endif
 };
 
 struct TileCoord {

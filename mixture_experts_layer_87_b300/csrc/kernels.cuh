@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(256, 1) route_topk_kernel(const float* __restr
                                                          const float* __restrict__ bias, int32_t* __restrict__ idx_out,
                                                          float* __restrict__ gate_out, int32_t* __restrict__ counts,
                                                          uint32_t* __restrict__ mask, int W, int group_size,
-                                                         int group_limit) {
+                                                         int group_limit, int* status) {
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -130,8 +130,10 @@ __global__ void __launch_bounds__(256, 1) route_topk_kernel(const float* __restr
   if (lane < k) {
     idx_out[(int64_t)t * k + lane] = my_idx;
     gate_out[(int64_t)t * k + lane] = gate;
-    atomicAdd(&counts[my_idx], 1);
-    if (mask) atomicOr(&mask[(int64_t)my_idx * W + (t >> 5)], 1u << (t & 31));
+    if (MOE_IN_RANGE(status, my_idx, E)) {
+      atomicAdd(&counts[my_idx], 1);
+      if (mask) atomicOr(&mask[(int64_t)my_idx * W + (t >> 5)], 1u << (t & 31));
+    }
   }
 }
 
@@ -292,7 +294,7 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
     const int32_t* __restrict__ idx, int T, int k, int E, const uint32_t* __restrict__ mask,
     const int32_t* __restrict__ wprefix, int W, const int32_t* __restrict__ offsets, int32_t* __restrict__ slot,
     int32_t* __restrict__ perm, const __nv_bfloat16* __restrict__ u, int d, void* __restrict__ x_perm,
-    float* __restrict__ x_scale, int64_t rows, uint8_t* __restrict__ uq, float* __restrict__ uq_scale) {
+    float* __restrict__ x_scale, int64_t rows, uint8_t* __restrict__ uq, float* __restrict__ uq_scale, int* status) {
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -303,8 +305,9 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
       const int w = t >> 5, b = t & 31;
       const int rank = wprefix[(int64_t)e * W + w] + __popc(mask[(int64_t)e * W + w] & ((1u << b) - 1u));
       my_slot = offsets[e] + rank;
+      if (!MOE_IN_RANGE(status, my_slot, rows)) my_slot = -1;
       slot[(int64_t)t * k + lane] = my_slot;
-      perm[my_slot] = t;
+      if (my_slot >= 0) perm[my_slot] = t;
     } else {
       slot[(int64_t)t * k + lane] = -1;
     }

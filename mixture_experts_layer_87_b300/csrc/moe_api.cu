@@ -227,7 +227,7 @@ moe_status enqueue_route(const moe_dims& d, const uint16_t* u, const uint16_t* c
 #define MOE_TOPK(V)                                                                                              \
   route_topk_kernel<V><<<blocks, 256, 0, st>>>(z, sp.splits, a.split_stride, d.T, d.E, d.k, bias, idx, gate, counts, \
                                                mask, W, d.route_groups > 0 ? d.E / d.route_groups : 0,            \
-                                               d.route_group_limit)
+                                               d.route_group_limit, status)
   if (vpl <= 1) MOE_TOPK(1);
   else if (vpl <= 2) MOE_TOPK(2);
   else if (vpl <= 4) MOE_TOPK(4);
@@ -259,10 +259,10 @@ moe_status enqueue_dispatch(const moe_dims& d, const int32_t* idx, const uint16_
   const __nv_bfloat16* ub = reinterpret_cast<const __nv_bfloat16*>(u);
   if (d.prec == MOE_FP8_E4M3)
     dispatch_kernel<true><<<blocks, 256, 0, st>>>(idx, d.T, d.k, d.E, mask, wprefix, W, offsets, slot, perm, ub, d.d,
-                                                  x, xs, rows, uq, uqs);
+                                                  x, xs, rows, uq, uqs, status);
   else
     dispatch_kernel<false><<<blocks, 256, 0, st>>>(idx, d.T, d.k, d.E, mask, wprefix, W, offsets, slot, perm, ub,
-                                                   d.d, x, nullptr, rows, nullptr, nullptr);
+                                                   d.d, x, nullptr, rows, nullptr, nullptr, status);
   MOE_TRY(launched());
   return rec ? rec->mark() : MOE_OK;
 }
@@ -384,6 +384,10 @@ moe_status enqueue_ffn_fp8(const moe_dims& d, const FfnOperands& o, int n_groups
   a.b_scale = o.w13s;
   a.out_scale = o.hs;
   a.out_scale_ld = o.rows_cap;
+#ifdef MOE_CHECK
+  a.b_rows = weight_experts(o, n_groups) * 2 * I;
+  a.out_rows = static_cast<int32_t>(o.rows_cap);
+#endif
   const bool few_rows = (table ? o.rows_cap : int64_t(uni_m) * n_groups) < 64 * int64_t(n_groups);
   MOE_TRY((launch_fp8<Epi::SWIGLU>(ta1, tb1, a, mt * (2 * I / 256), few_rows, st)));
   if (rec) MOE_TRY(rec->mark());
@@ -401,6 +405,9 @@ moe_status enqueue_ffn_fp8(const moe_dims& d, const FfnOperands& o, int n_groups
   b.a_scale_ld = o.rows_cap;
   b.b_scale = o.w2s;
   b.out_scale = nullptr;
+#ifdef MOE_CHECK
+  b.b_rows = weight_experts(o, n_groups) * D;
+#endif
   MOE_TRY((launch_fp8<Epi::BF16>(ta2, tb2, b, mt * cdiv(D, 256), few_rows, st)));
   return rec ? rec->mark() : MOE_OK;
 }
@@ -439,6 +446,10 @@ moe_status enqueue_ffn(const moe_dims& d, const FfnOperands& o, int n_groups, co
   a.x_rows = static_cast<int32_t>(o.x_rows);
   a.out = o.h;
   a.out_ld = I;
+#ifdef MOE_CHECK
+  a.w_rows = weight_experts(o, n_groups) * 2 * I;
+  a.out_rows = static_cast<int32_t>(o.rows_cap);
+#endif
   MOE_TRY((launch_xgemm<Epi::SWIGLU>(tw1, tx1, a, chunks * cdiv(2 * I, 256), st)));
   if (rec) MOE_TRY(rec->mark());
 
@@ -450,6 +461,9 @@ moe_status enqueue_ffn(const moe_dims& d, const FfnOperands& o, int n_groups, co
   b.x_rows = static_cast<int32_t>(o.rows_cap);
   b.out = o.y;
   b.out_ld = D;
+#ifdef MOE_CHECK
+  b.w_rows = weight_experts(o, n_groups) * D;
+#endif
   MOE_TRY((launch_xgemm<Epi::BF16>(tw2, tx2, b, chunks * cdiv(D, 256), st)));
   return rec ? rec->mark() : MOE_OK;
 }
@@ -479,6 +493,7 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_CUDA: return "CUDA runtime error";
     case MOE_ERR_TIMEOUT: return "device wait timed out";
     case MOE_ERR_BAD_INDEX: return "expert index or offset out of range";
+    case MOE_ERR_OUT_OF_RANGE: return "index outside its buffer (range-checked build)";
   }
   return "unknown status";
 }

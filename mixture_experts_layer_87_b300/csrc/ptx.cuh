@@ -10,7 +10,7 @@
 namespace moe {
 
 // Status word codes (mirror moe_status in include/moe.h).
-enum : int { ST_OK = 0, ST_TIMEOUT = 5, ST_BAD_INDEX = 6 };
+enum : int { ST_OK = 0, ST_TIMEOUT = 5, ST_BAD_INDEX = 6, ST_OUT_OF_RANGE = 7 };
 
 // Limit of one bounded wait inside the pipelined kernels.  A tile's longest
 // legitimate wait (the epilogue waiting for a whole K loop) is well under a
@@ -30,6 +30,22 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 __device__ __forceinline__ void record_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
+
+// Range-checked build (compiled with -DMOE_CHECK): MOE_IN_RANGE(status, i, n)
+// is true when 0 <= i < n; otherwise it records ST_OUT_OF_RANGE and is false,
+// and the guarded access is skipped.  Every computed index of a global load,
+// store or TMA coordinate of the kernels goes through it.  In the normal
+// build it is the constant true and costs nothing.
+__device__ __forceinline__ bool index_in_range(int* status, int64_t i, int64_t n) {
+  if (i >= 0 && i < n) return true;
+  record_status(status, ST_OUT_OF_RANGE);
+  return false;
+}
+#ifdef MOE_CHECK
+#define MOE_IN_RANGE(status, i, n) ::moe::index_in_range((status), static_cast<int64_t>(i), static_cast<int64_t>(n))
+#else
+#define MOE_IN_RANGE(status, i, n) true
+#endif
 
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -110,3 +110,14 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(capi, "LIB_PATH", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError, match="not built"):
         capi.lib()
+
+
+def test_range_checked_build_exports_the_same_symbols():
+    """The -DMOE_CHECK variant (every computed global index range-checked
+    into the status word) builds and exports the same C ABI."""
+    so = build.build(check=True)
+    L = ctypes.CDLL(so)
+    for n in capi.EXPORTS:
+        assert hasattr(L, n), n
+    L.moe_status_string.restype = ctypes.c_char_p
+    assert b"range-checked" in L.moe_status_string(7)
