@@ -204,7 +204,7 @@ def stage_work(cfg, counts: np.ndarray):
     """Algorithmic FLOPs and bytes of every stage of one forward (padding and
     repeated reads excluded)."""
     T, d, E, k, Ns, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.n_shared, cfg.inter
-    fp8 = cfg.prec == "fp8"
+    fp8 = cfg.is_fp8
     wb, xb = (1, 1) if fp8 else (2, 2)
     R = T * k
     active = int((counts > 0).sum())
@@ -230,7 +230,7 @@ def stage_work(cfg, counts: np.ndarray):
 def layer_work(cfg, counts):
     """The layer's algorithmic FLOPs and bytes (weights of the experts used, u in, h' out)."""
     T, d, E, k, Ns, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.n_shared, cfg.inter
-    fp8 = cfg.prec == "fp8"
+    fp8 = cfg.is_fp8
     wb = 1 if fp8 else 2
     active = int((counts > 0).sum())
     F = 2 * T * d * E + 2 * T * (k + Ns) * 3 * d * I
@@ -370,7 +370,7 @@ def oracle_sample(cfg, u_host, sample, cache=None):
     t0 = time.perf_counter()
     r = oracle.route(ub, cent, bias, cfg.k)
     oracle.layer_output(ub, np.arange(len(sample)), r["idx"], r["gate"], getter(False), getter(True),
-                        cfg.n_shared, cfg.E, fp8=cfg.prec == "fp8")
+                        cfg.n_shared, cfg.E, fp8=cfg.oracle_fp8)
     return time.perf_counter() - t0 - gen[0]
 
 
@@ -555,7 +555,8 @@ def main():
     ap.add_argument("--workload", default="v3", choices=["v3", "v3_fp8", "mid", "decode", "v3_slice", "v3_slice_fp8",
                                                             "decode_slice", "v3_tokens", "v3_tokens_fp8"])
     ap.add_argument("--no-variants", action="store_true", help="skip the mid, FP8 and decode measurements")
-    ap.add_argument("--prec", default=None, choices=["bf16", "fp8"], help="override the workload's precision")
+    ap.add_argument("--prec", default=None, choices=["bf16", "fp8", "fp8_ue8m0"],
+                    help="override the workload's precision")
     ap.add_argument("--cpu-tokens", type=int, default=512, help="tokens in the CPU-oracle baseline sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--ref-tokens", type=int, default=0,

@@ -61,7 +61,14 @@ typedef enum {
                                its buffer; the access was skipped */
 } moe_status;
 
-typedef enum { MOE_BF16 = 0, MOE_FP8_E4M3 = 1 } moe_precision;
+/* Precision of the expert GEMMs.  MOE_FP8_UE8M0: the FP8 scheme with UE8M0
+ * scales -- the scheme DeepSeek-V3.1 moved to (ai.flicky.cc, continuation of
+ * section 3.5): every scale a power of two (an 8-bit exponent, no mantissa),
+ * taken as amax/448 rounded up to the next power of two, so that no element
+ * of a group exceeds 448 after scaling; everything else as MOE_FP8_E4M3 (the
+ * weights must be quantised with power-of-two scales too, see
+ * moe_quantize_fp8_blocks). */
+typedef enum { MOE_BF16 = 0, MOE_FP8_E4M3 = 1, MOE_FP8_UE8M0 = 2 } moe_precision;
 
 /* Layer shape.  T tokens, hidden size d, E routed experts, k of them per
  * token, n_shared shared experts, SwiGLU intermediate size inter (= I) of
@@ -307,12 +314,13 @@ moe_status moe_forward_profiled(const moe_dims* dims, const moe_weights* w, cons
  * moe_quantize_fp8_blocks: w [rows, cols] bf16 -> q [rows, cols] E4M3 codes and
  *   scale [rows/128, cols/128] fp32 with scale = amax/448 of each 128 x 128 block
  *   (1 for an all-zero block), q = round-to-nearest-even, saturating, of w/scale
- *   (ai.flicky.cc 3.3 item 2).  rows and cols multiples of 128.
+ *   (ai.flicky.cc 3.3 item 2).  rows and cols multiples of 128.  pow2_scales
+ *   != 0: the scale rounded up to a power of two (UE8M0, MOE_FP8_UE8M0).
  */
 moe_status moe_pack_gate_up(const uint16_t* w1, const uint16_t* w3, int32_t E, int32_t inter, int32_t d,
                             uint16_t* w13, void* stream);
 moe_status moe_quantize_fp8_blocks(const uint16_t* w, int64_t rows, int32_t cols, uint8_t* q, float* scale,
-                                   void* stream);
+                                   int32_t pow2_scales, void* stream);
 
 /* Synchronises `stream` and returns the device status word of workspace `ws`
  * (MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_BAD_INDEX), or MOE_ERR_CUDA if the stream

@@ -18,7 +18,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmoe_b300_check.so" if os.environ.get("MOE_B300_LIBRARY") == "check"
                         else "libmoe_b300.so")
 
-MOE_BF16, MOE_FP8_E4M3 = 0, 1
+MOE_BF16, MOE_FP8_E4M3, MOE_FP8_UE8M0 = 0, 1, 2
 
 # Every symbol include/moe.h declares.
 EXPORTS = (
@@ -77,7 +77,7 @@ def lib() -> ctypes.CDLL:
                                        ctypes.c_int),
             "moe_plan_replicas": ([i32, vp, i32, vp, vp, vp], ctypes.c_int),
             "moe_pack_gate_up": ([vp, vp, i32, i32, i32, vp, vp], ctypes.c_int),
-            "moe_quantize_fp8_blocks": ([vp, i64, i32, vp, vp, vp], ctypes.c_int),
+            "moe_quantize_fp8_blocks": ([vp, i64, i32, vp, vp, i32, vp], ctypes.c_int),
             "moe_read_device_status": ([vp, vp], ctypes.c_int),
             "moe_selftest_wait_timeout": ([vp, sz, i32, vp], ctypes.c_int),
         }
@@ -116,7 +116,7 @@ def _stream(stream):
 
 
 def dims(T, d, E, k, n_shared, inter, prec, route_groups=0, route_group_limit=0) -> moe_dims:
-    p = {"bf16": MOE_BF16, "fp8": MOE_FP8_E4M3}.get(prec, prec)
+    p = {"bf16": MOE_BF16, "fp8": MOE_FP8_E4M3, "fp8_ue8m0": MOE_FP8_UE8M0}.get(prec, prec)
     return moe_dims(int(T), int(d), int(E), int(k), int(n_shared), int(inter), int(p), int(route_groups),
                     int(route_group_limit))
 
@@ -221,8 +221,9 @@ def moe_pack_gate_up(w1, w3, E, inter, d, w13, stream=None):
            "moe_pack_gate_up")
 
 
-def moe_quantize_fp8_blocks(w, rows, cols, q, scale, stream=None):
-    _check(lib().moe_quantize_fp8_blocks(_ptr(w), int(rows), int(cols), _ptr(q), _ptr(scale), _stream(stream)),
+def moe_quantize_fp8_blocks(w, rows, cols, q, scale, stream=None, pow2_scales=False):
+    _check(lib().moe_quantize_fp8_blocks(_ptr(w), int(rows), int(cols), _ptr(q), _ptr(scale), int(bool(pow2_scales)),
+                                         _stream(stream)),
            "moe_quantize_fp8_blocks")
 
 

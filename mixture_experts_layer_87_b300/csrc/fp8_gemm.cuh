@@ -176,7 +176,10 @@ __device__ __forceinline__ void fma2(uint64_t& a, uint32_t v0, uint32_t v1, uint
 __device__ __forceinline__ float lo_of(uint64_t a) { return __uint_as_float(static_cast<uint32_t>(a)); }
 __device__ __forceinline__ float hi_of(uint64_t a) { return __uint_as_float(static_cast<uint32_t>(a >> 32)); }
 
-template <Epi EPI, int EW>
+// POW2: the SwiGLU epilogue quantises h with UE8M0 scales (amax/448 rounded up
+// to a power of two); a template flag, since one more argument word costs the
+// 16-warp epilogue a register spill.
+template <Epi EPI, int EW, bool POW2 = false>
 __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
     fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmArgs args) {
@@ -495,7 +498,8 @@ __global__ void __launch_bounds__(F8Shape<EW>::THREADS, 1)
         if (!ok) break;
 #pragma unroll
         for (int c = 0; c < CG; ++c) amax = fmaxf(amax, ax[c * 128 + r]);
-        const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+        float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+        if constexpr (POW2) scale = pow2_ceil(scale);
         // h is a GEMM output known to fp32 accuracy: its codes are taken from
         // h * (1/scale), one correctly rounded reciprocal per row
         const float inv = 1.0f / scale;

@@ -87,6 +87,17 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&
   }
 }
 
+// UE8M0 scale (DeepSeek-V3.1's FP8 scales are bare powers of two,
+// ai.flicky.cc in its continuation of section 3.5): the smallest power of two
+// >= s for a positive finite fp32 s -- s itself when its mantissa bits are
+// zero, else the next exponent; scales below 2^-126 become 2^-126.
+__device__ __forceinline__ float pow2_ceil(float s) {
+  constexpr float kMinNormal = 1.17549435e-38f;  // 2^-126
+  if (!(s > kMinNormal)) return kMinNormal;
+  const uint32_t b = __float_as_uint(s);
+  return (b & 0x7FFFFFu) ? __uint_as_float((b & 0x7F800000u) + 0x00800000u) : s;
+}
+
 // Two fp32 -> two E4M3 codes, round-to-nearest-even, saturating (cvt.rn.satfinite).
 __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
   return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));

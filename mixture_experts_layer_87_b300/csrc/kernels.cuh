@@ -294,7 +294,8 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
     const int32_t* __restrict__ idx, int T, int k, int E, const uint32_t* __restrict__ mask,
     const int32_t* __restrict__ wprefix, int W, const int32_t* __restrict__ offsets, int32_t* __restrict__ slot,
     int32_t* __restrict__ perm, const __nv_bfloat16* __restrict__ u, int d, void* __restrict__ x_perm,
-    float* __restrict__ x_scale, int64_t rows, uint8_t* __restrict__ uq, float* __restrict__ uq_scale, int* status) {
+    float* __restrict__ x_scale, int64_t rows, uint8_t* __restrict__ uq, float* __restrict__ uq_scale, int* status,
+    bool pow2) {
   const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (t >= T) return;
@@ -346,7 +347,8 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
       }
 #pragma unroll
       for (int off = 4; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      const float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+      float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+      if (pow2) scale = pow2_ceil(scale);  // UE8M0 scales
       uint4 code = make_uint4(0, 0, 0, 0);
       if (active) {
         uint32_t c8[8];
@@ -440,9 +442,11 @@ __global__ void bias_update_kernel(int E, int64_t T, int k, const int32_t* __res
 
 // ---------------------------------------------------------------------------
 // Offline: 128 x 128 block quantisation of bf16 weights to E4M3 (ai.flicky.cc
-// 3.3 item 2).  One block of 256 threads per 128 x 128 block.
+// 3.3 item 2).  One block of 256 threads per 128 x 128 block.  pow2: UE8M0
+// scales (amax/448 rounded up to a power of two).
 __global__ void __launch_bounds__(256) quantize_blocks_kernel(const __nv_bfloat16* __restrict__ w, int cols,
-                                                              uint8_t* __restrict__ q, float* __restrict__ scale) {
+                                                              uint8_t* __restrict__ q, float* __restrict__ scale,
+                                                              bool pow2) {
   __shared__ float red[8];
   const int bc = blockIdx.x, br = blockIdx.y;
   const int64_t row0 = (int64_t)br * 128;
@@ -464,7 +468,8 @@ __global__ void __launch_bounds__(256) quantize_blocks_kernel(const __nv_bfloat1
   amax = red[0];
 #pragma unroll
   for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
-  const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+  float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+  if (pow2) s = pow2_ceil(s);
   if (threadIdx.x == 0) scale[(int64_t)br * (cols / 128) + bc] = s;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {

@@ -25,6 +25,9 @@ namespace {
 constexpr size_t kAlign = 256;
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
+// E4M3 expert GEMMs, with amax/448 scales or with UE8M0 (power-of-two) scales.
+bool is_fp8(const moe_dims& d) { return d.prec == MOE_FP8_E4M3 || d.prec == MOE_FP8_UE8M0; }
+
 // Entries of the chunk -> group table: at most rows/128 + one partial chunk
 // per group (chunks are >= 128 rows).
 int64_t cgroup_cap(const moe_dims& d) {
@@ -68,7 +71,7 @@ Layout make_layout(const moe_dims& d) {
     return o;
   };
   const int64_t T = d.T, R = T * d.k, W = (T + 31) / 32, E = d.E, I = d.inter, D = d.d, Ns = d.n_shared;
-  const bool fp8 = d.prec == MOE_FP8_E4M3;
+  const bool fp8 = is_fp8(d);
   const int64_t eb = fp8 ? 1 : 2;  // bytes per GEMM operand element
   L.status = take(256);
   L.queue = take(4 * sizeof(int));  // item counters of the four expert GEMM launches
@@ -110,7 +113,7 @@ bool d_T_nonzero(const moe_dims* d) { return d->T != 0; }
 moe_status check_dims(const moe_dims* d) {
   if (!d) return MOE_ERR_INVALID_ARG;
   if (d->T < 0 || d->d <= 0 || d->E <= 0 || d->k <= 0 || d->n_shared < 0 || d->inter <= 0) return MOE_ERR_INVALID_ARG;
-  if (d->prec != MOE_BF16 && d->prec != MOE_FP8_E4M3) return MOE_ERR_INVALID_ARG;
+  if (d->prec != MOE_BF16 && d->prec != MOE_FP8_E4M3 && d->prec != MOE_FP8_UE8M0) return MOE_ERR_INVALID_ARG;
   if (d->k > d->E || d->k > 32) return MOE_ERR_INVALID_ARG;
   if (d->E > 1024) return MOE_ERR_UNSUPPORTED;
   if (d->d % 128 != 0 || d->inter % 128 != 0) return MOE_ERR_UNSUPPORTED;
@@ -193,7 +196,7 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // Token rows per chunk of the expert GEMMs (the N of one MMA at most).
 constexpr int kChunkBf16 = kXChunk;
 constexpr int kChunkFp8 = 128;
-int chunk_rows(const moe_dims& d) { return d.prec == MOE_FP8_E4M3 ? kChunkFp8 : kChunkBf16; }
+int chunk_rows(const moe_dims& d) { return is_fp8(d) ? kChunkFp8 : kChunkBf16; }
 
 // ------------------------------------------------------------------ pieces
 // Router logits (tcgen05 GEMM, bf16 in, fp32 out) then the warp-per-token top-k.
@@ -257,12 +260,12 @@ moe_status enqueue_dispatch(const moe_dims& d, const int32_t* idx, const uint16_
   const unsigned blocks = static_cast<unsigned>(cdiv(int64_t(d.T) * 32, 256));
   const int64_t rows = int64_t(d.T) * d.k;
   const __nv_bfloat16* ub = reinterpret_cast<const __nv_bfloat16*>(u);
-  if (d.prec == MOE_FP8_E4M3)
+  if (is_fp8(d))
     dispatch_kernel<true><<<blocks, 256, 0, st>>>(idx, d.T, d.k, d.E, mask, wprefix, W, offsets, slot, perm, ub, d.d,
-                                                  x, xs, rows, uq, uqs, status);
+                                                  x, xs, rows, uq, uqs, status, d.prec == MOE_FP8_UE8M0);
   else
     dispatch_kernel<false><<<blocks, 256, 0, st>>>(idx, d.T, d.k, d.E, mask, wprefix, W, offsets, slot, perm, ub,
-                                                   d.d, x, nullptr, rows, nullptr, nullptr, status);
+                                                   d.d, x, nullptr, rows, nullptr, nullptr, status, false);
   MOE_TRY(launched());
   return rec ? rec->mark() : MOE_OK;
 }
@@ -297,11 +300,11 @@ moe_status launch_xgemm(const CUtensorMap& tw, const CUtensorMap& tx, const XGem
   return launched();
 }
 
-template <Epi EPI, int EW>
+template <Epi EPI, int EW, bool POW2>
 moe_status launch_fp8_ew(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int64_t grid,
                          cudaStream_t st) {
   constexpr size_t smem = fp8_gemm_smem_bytes<EPI, EW>();
-  auto kern = fp8_gemm_kernel<EPI, EW>;
+  auto kern = fp8_gemm_kernel<EPI, EW, POW2>;
   // The kernel moves registers between its warpgroups (setmaxnreg); its split
   // adds up to exactly LAUNCH_REGS per thread, so a build that launched with
   // fewer would leave the epilogue warps waiting for registers forever.
@@ -318,12 +321,16 @@ moe_status launch_fp8_ew(const CUtensorMap& ta, const CUtensorMap& tb, const Gem
 // warps share it.
 template <Epi EPI>
 moe_status launch_fp8(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& a, int64_t items_bound,
-                      bool few_rows, cudaStream_t st) {
+                      bool few_rows, bool pow2, cudaStream_t st) {
   if (items_bound <= 0) return MOE_OK;
   int sms = 0;
   MOE_TRY(sm_count(&sms));
   const int64_t grid = items_bound < sms ? items_bound : sms;
-  return few_rows ? launch_fp8_ew<EPI, 16>(ta, tb, a, grid, st) : launch_fp8_ew<EPI, 8>(ta, tb, a, grid, st);
+  if constexpr (EPI == Epi::SWIGLU) {  // only the SwiGLU epilogue quantises (h), so only it has UE8M0 variants
+    if (pow2)
+      return few_rows ? launch_fp8_ew<EPI, 16, true>(ta, tb, a, grid, st) : launch_fp8_ew<EPI, 8, true>(ta, tb, a, grid, st);
+  }
+  return few_rows ? launch_fp8_ew<EPI, 16, false>(ta, tb, a, grid, st) : launch_fp8_ew<EPI, 8, false>(ta, tb, a, grid, st);
 }
 
 // Gate/up (+SwiGLU) then down GEMMs over a set of groups.
@@ -389,7 +396,7 @@ moe_status enqueue_ffn_fp8(const moe_dims& d, const FfnOperands& o, int n_groups
   a.out_rows = static_cast<int32_t>(o.rows_cap);
 #endif
   const bool few_rows = (table ? o.rows_cap : int64_t(uni_m) * n_groups) < 64 * int64_t(n_groups);
-  MOE_TRY((launch_fp8<Epi::SWIGLU>(ta1, tb1, a, mt * (2 * I / 256), few_rows, st)));
+  MOE_TRY((launch_fp8<Epi::SWIGLU>(ta1, tb1, a, mt * (2 * I / 256), few_rows, d.prec == MOE_FP8_UE8M0, st)));
   if (rec) MOE_TRY(rec->mark());
 
   GemmArgs b = a;
@@ -408,7 +415,7 @@ moe_status enqueue_ffn_fp8(const moe_dims& d, const FfnOperands& o, int n_groups
 #ifdef MOE_CHECK
   b.b_rows = weight_experts(o, n_groups) * D;
 #endif
-  MOE_TRY((launch_fp8<Epi::BF16>(ta2, tb2, b, mt * cdiv(D, 256), few_rows, st)));
+  MOE_TRY((launch_fp8<Epi::BF16>(ta2, tb2, b, mt * cdiv(D, 256), few_rows, false, st)));
   return rec ? rec->mark() : MOE_OK;
 }
 
@@ -417,7 +424,7 @@ moe_status enqueue_ffn_fp8(const moe_dims& d, const FfnOperands& o, int n_groups
 moe_status enqueue_ffn(const moe_dims& d, const FfnOperands& o, int n_groups, const GroupEntry* table,
                        const int32_t* ch_total, const int32_t* cgroup, int uni_m, int* queue, int* status,
                        cudaStream_t st, Recorder* rec = nullptr) {
-  if (d.prec == MOE_FP8_E4M3)
+  if (is_fp8(d))
     return enqueue_ffn_fp8(d, o, n_groups, table, ch_total, cgroup, uni_m, queue, status, st, rec);
   const int I = d.inter, D = d.d;
   constexpr int CH = kChunkBf16;
@@ -472,7 +479,7 @@ moe_status check_weights(const moe_dims& d, const moe_weights* w) {
   if (!w || !w->w13 || !w->w2 || !w->centroids) return MOE_ERR_INVALID_ARG;
   if (!aligned16(w->w13) || !aligned16(w->w2) || !aligned16(w->centroids)) return MOE_ERR_INVALID_ARG;
   if (d.n_shared > 0 && (!w->ws13 || !w->ws2 || !aligned16(w->ws13) || !aligned16(w->ws2))) return MOE_ERR_INVALID_ARG;
-  if (d.prec == MOE_FP8_E4M3) {
+  if (is_fp8(d)) {
     if (!w->w13_scale || !w->w2_scale) return MOE_ERR_INVALID_ARG;
     if (d.n_shared > 0 && (!w->ws13_scale || !w->ws2_scale)) return MOE_ERR_INVALID_ARG;
   }
@@ -529,7 +536,7 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, const uint
   // token-sized buffers may be empty (null) when T == 0
   const bool empty = dims->T == 0;
   if (!offsets || (!empty && (!topk_idx || !u || !perm || !slot || !x_perm))) return MOE_ERR_INVALID_ARG;
-  if (dims->prec == MOE_FP8_E4M3 && !empty && !x_scale) return MOE_ERR_INVALID_ARG;
+  if (is_fp8(*dims) && !empty && !x_scale) return MOE_ERR_INVALID_ARG;
   if (!aligned16(u) || !aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
   const Layout L = make_layout(*dims);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -555,7 +562,7 @@ moe_status moe_grouped_ffn(const moe_dims* dims, int32_t n_groups, int32_t rows,
                            const float* w2_scale, uint16_t* y, void* ws, size_t ws_bytes, void* stream) {
   MOE_TRY(check_dims(dims));
   MOE_TRY(check_ws(dims, ws, ws_bytes));
-  const bool fp8 = dims->prec == MOE_FP8_E4M3;
+  const bool fp8 = is_fp8(*dims);
   if (n_groups <= 0 || n_groups > dims->E + dims->n_shared || rows < 0) return MOE_ERR_INVALID_ARG;
   if (group_expert && n_weight_experts <= 0) return MOE_ERR_INVALID_ARG;
   if (int64_t(rows) > int64_t(dims->T) * dims->k) return MOE_ERR_WORKSPACE;
@@ -639,7 +646,7 @@ moe_status forward_impl(const moe_dims* dims, const moe_weights* w, const uint16
   if (!bias || (d_T_nonzero(dims) && (!u || !out)) || !aligned16(u) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
   if (events && n_events < MOE_PROFILE_EVENTS) return MOE_ERR_INVALID_ARG;
   const moe_dims& d = *dims;
-  const bool fp8 = d.prec == MOE_FP8_E4M3;
+  const bool fp8 = is_fp8(d);
   const Layout L = make_layout(wd);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   Recorder recorder;
@@ -765,7 +772,7 @@ moe_status moe_pack_gate_up(const uint16_t* w1, const uint16_t* w3, int32_t E, i
 }
 
 moe_status moe_quantize_fp8_blocks(const uint16_t* w, int64_t rows, int32_t cols, uint8_t* q, float* scale,
-                                   void* stream) {
+                                   int32_t pow2_scales, void* stream) {
   if (!w || !q || !scale || rows <= 0 || cols <= 0 || rows % 128 || cols % 128) return MOE_ERR_INVALID_ARG;
   if (rows / 128 > 65535 * 64) return MOE_ERR_UNSUPPORTED;
   if (!aligned16(w) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
@@ -775,7 +782,7 @@ moe_status moe_quantize_fp8_blocks(const uint16_t* w, int64_t rows, int32_t cols
     const int64_t r = rows - r0 < int64_t(65535) * 128 ? rows - r0 : int64_t(65535) * 128;
     dim3 grid(cols / 128, static_cast<unsigned>(r / 128));
     quantize_blocks_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(w) + r0 * cols, cols,
-                                                 q + r0 * cols, scale + (r0 / 128) * (cols / 128));
+                                                 q + r0 * cols, scale + (r0 / 128) * (cols / 128), pow2_scales != 0);
     MOE_TRY(launched());
   }
   return MOE_OK;

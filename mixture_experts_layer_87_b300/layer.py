@@ -21,7 +21,8 @@ class MoELayer:
         self.T, self.d, self.E, self.k, self.n_shared, self.inter, self.prec = T, d, E, k, n_shared, inter, prec
         self.route_groups, self.route_group_limit = route_groups, route_group_limit
         self.device = torch.device(device)
-        self.fp8 = prec == "fp8"
+        self.fp8 = prec in ("fp8", "fp8_ue8m0")
+        self.pow2 = prec == "fp8_ue8m0"   # UE8M0 (power-of-two) scales
         self.dims = capi.dims(T, d, E, k, n_shared, inter, prec, route_groups, route_group_limit)
         self.ws = torch.empty(capi.moe_workspace_size(self.dims), dtype=torch.uint8, device=self.device)
         wt = torch.uint8 if self.fp8 else torch.bfloat16
@@ -61,9 +62,9 @@ class MoELayer:
         capi.moe_pack_gate_up(self._stage13[0], self._stage13[1], 1, I, d, self._stage_pack)
         s13 = (self.ws13_scale if shared else self.w13_scale)[e]
         s2 = (self.ws2_scale if shared else self.w2_scale)[e]
-        capi.moe_quantize_fp8_blocks(self._stage_pack, 2 * I, d, w13, s13)
+        capi.moe_quantize_fp8_blocks(self._stage_pack, 2 * I, d, w13, s13, pow2_scales=self.pow2)
         self._stage2.copy_(w2)
-        capi.moe_quantize_fp8_blocks(self._stage2, d, I, w2d, s2)
+        capi.moe_quantize_fp8_blocks(self._stage2, d, I, w2d, s2, pow2_scales=self.pow2)
 
     def release_staging(self) -> None:
         torch.cuda.current_stream().synchronize()

@@ -55,8 +55,8 @@ def _load():
         lib.oracle_e4m3_decode.restype = ctypes.c_double
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
-        lib.oracle_quant_1x128.argtypes = [i64, i32, vp, vp, vp]
-        lib.oracle_quant_128x128.argtypes = [i64, i32, vp, vp, vp]
+        lib.oracle_quant_1x128.argtypes = [i64, i32, vp, vp, vp, i32]
+        lib.oracle_quant_128x128.argtypes = [i64, i32, vp, vp, vp, i32]
         lib.oracle_swiglu.argtypes = [i64, i32, i32, vp, vp, vp, vp, i32, vp]
         lib.oracle_bias_update.argtypes = [i32, i64, i32, vp, f32, vp]
         _lib = lib
@@ -159,25 +159,27 @@ def e4m3_decode(q: np.ndarray) -> np.ndarray:
     return table[flat].reshape(np.shape(q))
 
 
-def quant_1x128(x: np.ndarray):
-    """1 x 128 activation tiles along the last axis: (codes uint8, scales fp32 [rows, cols/128])."""
+def quant_1x128(x: np.ndarray, pow2: bool = False):
+    """1 x 128 activation tiles along the last axis: (codes uint8, scales fp32 [rows, cols/128]).
+    pow2: UE8M0 scales (amax/448 rounded up to a power of two)."""
     x = _c(x, np.float64)
     rows, cols = x.shape
     assert cols % 128 == 0
     q = np.empty((rows, cols), np.uint8)
     s = np.empty((rows, cols // 128), np.float32)
-    _load().oracle_quant_1x128(rows, cols, x.ctypes.data, q.ctypes.data, s.ctypes.data)
+    _load().oracle_quant_1x128(rows, cols, x.ctypes.data, q.ctypes.data, s.ctypes.data, int(pow2))
     return q, s
 
 
-def quant_128x128(w: np.ndarray):
-    """128 x 128 weight blocks: (codes uint8, scales fp32 [rows/128, cols/128])."""
+def quant_128x128(w: np.ndarray, pow2: bool = False):
+    """128 x 128 weight blocks: (codes uint8, scales fp32 [rows/128, cols/128]).
+    pow2: UE8M0 scales (amax/448 rounded up to a power of two)."""
     w = _c(w, np.float64)
     rows, cols = w.shape
     assert rows % 128 == 0 and cols % 128 == 0
     q = np.empty((rows, cols), np.uint8)
     s = np.empty((rows // 128, cols // 128), np.float32)
-    _load().oracle_quant_128x128(rows, cols, w.ctypes.data, q.ctypes.data, s.ctypes.data)
+    _load().oracle_quant_128x128(rows, cols, w.ctypes.data, q.ctypes.data, s.ctypes.data, int(pow2))
     return q, s
 
 
@@ -189,18 +191,19 @@ def dequant_128x128(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     return e4m3_decode(q) * np.repeat(np.repeat(s.astype(np.float64), 128, axis=0), 128, axis=1)
 
 
-def fp8_roundtrip_1x128(x: np.ndarray) -> np.ndarray:
-    return dequant_1x128(*quant_1x128(x))
+def fp8_roundtrip_1x128(x: np.ndarray, pow2: bool = False) -> np.ndarray:
+    return dequant_1x128(*quant_1x128(x, pow2))
 
 
-def fp8_roundtrip_128x128(w: np.ndarray) -> np.ndarray:
-    return dequant_128x128(*quant_128x128(w))
+def fp8_roundtrip_128x128(w: np.ndarray, pow2: bool = False) -> np.ndarray:
+    return dequant_128x128(*quant_128x128(w, pow2))
 
 
 # ----------------------------------------------------------------------------
 # expert FFN and the layer
-def swiglu(x: np.ndarray, w1: np.ndarray, w3: np.ndarray, w2: np.ndarray, h_quant: bool = False) -> np.ndarray:
-    """y = W2 (SiLU(W1 x) * (W3 x)) per row, fp64 (three d x I matrices: ai.flicky.cc exercise)."""
+def swiglu(x: np.ndarray, w1: np.ndarray, w3: np.ndarray, w2: np.ndarray, h_quant=False) -> np.ndarray:
+    """y = W2 (SiLU(W1 x) * (W3 x)) per row, fp64 (three d x I matrices: ai.flicky.cc exercise).
+    h_quant: False, True (h quantised per 1 x 128 tile, amax/448 scales) or "ue8m0" (UE8M0 scales)."""
     x, w1, w3, w2 = (_c(a, np.float64) for a in (x, w1, w3, w2))
     n, d = x.shape
     I = w1.shape[0]
@@ -208,20 +211,21 @@ def swiglu(x: np.ndarray, w1: np.ndarray, w3: np.ndarray, w2: np.ndarray, h_quan
     y = np.empty((n, d), np.float64)
     if n:
         _load().oracle_swiglu(n, d, I, x.ctypes.data, w1.ctypes.data, w3.ctypes.data, w2.ctypes.data,
-                              int(h_quant), y.ctypes.data)
+                              2 if h_quant == "ue8m0" else int(bool(h_quant)), y.ctypes.data)
     return y
 
 
-def expert_operands(w1_bits, w3_bits, w2_bits, fp8: bool):
-    """fp64 operands of one expert: the bf16 weights, or their 128x128-block FP8 round trip."""
+def expert_operands(w1_bits, w3_bits, w2_bits, fp8):
+    """fp64 operands of one expert: the bf16 weights, or their 128x128-block FP8
+    round trip (fp8 = True: amax/448 scales; fp8 = "ue8m0": UE8M0 scales)."""
     ws = [bf16_to_f64(w) for w in (w1_bits, w3_bits, w2_bits)]
     if fp8:
-        ws = [fp8_roundtrip_128x128(w) for w in ws]
+        ws = [fp8_roundtrip_128x128(w, pow2=fp8 == "ue8m0") for w in ws]
     return ws
 
 
 def layer_output(u_bits: np.ndarray, tokens: np.ndarray, idx: np.ndarray, gate: np.ndarray,
-                 routed_weights, shared_weights, n_shared: int, E: int, fp8: bool = False) -> np.ndarray:
+                 routed_weights, shared_weights, n_shared: int, E: int, fp8=False) -> np.ndarray:
     """h'_t = u_t + sum_s FFN_s(u_t) + sum_j g_{t,j} FFN_{S_j}(u_t) for the given tokens, fp64.
 
     The layer equation of ai.flicky.cc 2.1.2 / xyznot.com Method 2.  idx and
@@ -230,11 +234,12 @@ def layer_output(u_bits: np.ndarray, tokens: np.ndarray, idx: np.ndarray, gate: 
     at a time (expert-major), so only one expert's fp64 copy is alive.
     fp8=True: every main-GEMM input is its FP8 round trip (weights 128x128
     blocks, u and h 1x128 tiles; the router stays high precision, 3.3 item 1);
-    the residual u is the layer input itself.
+    the residual u is the layer input itself.  fp8="ue8m0": the same with
+    UE8M0 scales (powers of two) in every quantisation.
     """
     tokens = np.asarray(tokens, np.int64)
     u_rows = bf16_to_f64(u_bits[tokens])
-    x = fp8_roundtrip_1x128(u_rows) if fp8 else u_rows
+    x = fp8_roundtrip_1x128(u_rows, pow2=fp8 == "ue8m0") if fp8 else u_rows
     out = u_rows.copy()
     for s in range(n_shared):
         w1, w3, w2 = expert_operands(*shared_weights(s), fp8)
@@ -250,7 +255,7 @@ def layer_output(u_bits: np.ndarray, tokens: np.ndarray, idx: np.ndarray, gate: 
 
 
 def expert_rows(u_bits: np.ndarray, tokens: np.ndarray, idx: np.ndarray, routed_weights, shared_weights,
-                n_shared: int, E: int, fp8: bool = False):
+                n_shared: int, E: int, fp8=False):
     """The expert outputs layer_output sums, kept apart, fp64.
 
     Returns (y [n, k, d], ysh [N_s, n, d]) for the n given tokens:
@@ -262,7 +267,7 @@ def expert_rows(u_bits: np.ndarray, tokens: np.ndarray, idx: np.ndarray, routed_
     """
     tokens = np.asarray(tokens, np.int64)
     u_rows = bf16_to_f64(u_bits[tokens])
-    x = fp8_roundtrip_1x128(u_rows) if fp8 else u_rows
+    x = fp8_roundtrip_1x128(u_rows, pow2=fp8 == "ue8m0") if fp8 else u_rows
     n, k = idx.shape
     d = u_rows.shape[1]
     y = np.zeros((n, k, d))

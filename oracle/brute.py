@@ -97,22 +97,33 @@ def e4m3_round(x: np.ndarray) -> np.ndarray:
     return np.copysign(vals[pick], x)
 
 
-def quant_dequant(x: np.ndarray, group_rows: int, group_cols: int) -> np.ndarray:
+def pow2_at_least(s: np.ndarray) -> np.ndarray:
+    """The smallest power of two >= s, for positive fp32 s (numpy's frexp:
+    s = m 2^e with m in [0.5, 1); s is a power of two exactly when m = 0.5)."""
+    m, e = np.frexp(np.asarray(s, np.float32))
+    return np.where(m == 0.5, s, np.ldexp(np.float32(1.0), e)).astype(np.float32)
+
+
+def quant_dequant(x: np.ndarray, group_rows: int, group_cols: int, pow2: bool = False) -> np.ndarray:
     """Quantise x [R, C] in groups of group_rows x group_cols elements and
     return the dequantised values: scale = amax / 448 in fp32 (1 for an
-    all-zero group), element = nearest E4M3 of (x / scale) taken in fp32,
-    times scale."""
+    all-zero group) -- rounded up to a power of two for UE8M0 scales (pow2) --,
+    element = nearest E4M3 of (x / scale) taken in fp32, times scale."""
     x = np.asarray(x, np.float64)
     R, C = x.shape
     g = x.reshape(R // group_rows, group_rows, C // group_cols, group_cols)
     amax = np.abs(g).max(axis=(1, 3), keepdims=True)
     scale = np.where(amax > 0, amax.astype(np.float32) / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    if pow2:
+        scale = pow2_at_least(scale)
     ratio = (g.astype(np.float32) / scale).astype(np.float64)
     return (e4m3_round(ratio) * scale.astype(np.float64)).reshape(R, C)
 
 
-def dense_layer_fp8(u: np.ndarray, cent: np.ndarray, bias: np.ndarray, k: int, routed, shared) -> dict:
-    """The layer of dense_layer with the FP8 operands of the main GEMMs.
+def dense_layer_fp8(u: np.ndarray, cent: np.ndarray, bias: np.ndarray, k: int, routed, shared,
+                    pow2: bool = False) -> dict:
+    """The layer of dense_layer with the FP8 operands of the main GEMMs
+    (pow2: every scale a power of two, the UE8M0 scales of DeepSeek-V3.1).
 
     Routing (affinities, selection, gates) uses the unquantised u; every
     expert, shared or routed, multiplies the 1 x 128-quantised u by its
@@ -128,12 +139,12 @@ def dense_layer_fp8(u: np.ndarray, cent: np.ndarray, bias: np.ndarray, k: int, r
         for i in order[:k]:
             g[t, i] = s[t, i]
         g[t] /= g[t].sum()
-    xq = quant_dequant(u, 1, 128)
+    xq = quant_dequant(u, 1, 128, pow2)
 
     def expert(w1, w3, w2):
-        w1q, w3q, w2q = (quant_dequant(w, 128, 128) for w in (w1, w3, w2))
+        w1q, w3q, w2q = (quant_dequant(w, 128, 128, pow2) for w in (w1, w3, w2))
         h = _silu_and_mul(xq @ w1q.T, xq @ w3q.T)
-        return quant_dequant(h, 1, 128) @ w2q.T
+        return quant_dequant(h, 1, 128, pow2) @ w2q.T
 
     out = u.copy()
     for ws in shared:

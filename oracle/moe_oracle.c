@@ -172,6 +172,24 @@ static float group_scale(double amax) {
   return (float)amax / 448.0f;
 }
 
+/*
+ * UE8M0 scales (ai.flicky.cc, continuation of section 3.5: DeepSeek-V3.1 moved
+ * to FP8 with UE8M0 scales, a scale that is a bare 8-bit exponent).  The page
+ * gives no rounding rule; reading: the amax/448 scale above rounded UP to a
+ * power of two, so that no element of the group exceeds 448 after scaling.
+ * frexpf splits s = f * 2^e with f in [0.5, 1); s is a power of two exactly
+ * when f == 0.5.  Scales below 2^-126 (never met by bf16 data) become 2^-126.
+ */
+static float group_scale_pow2(double amax) {
+  const float s = group_scale(amax);
+  if (s <= ldexpf(1.0f, -126)) return ldexpf(1.0f, -126);
+  int e;
+  const float f = frexpf(s, &e);
+  return f == 0.5f ? s : ldexpf(1.0f, e);
+}
+
+static float scale_of(double amax, int pow2) { return pow2 ? group_scale_pow2(amax) : group_scale(amax); }
+
 /* Code of one element: x / scale rounded to fp32 (the kernels' precision), then E4M3. */
 static uint8_t quant_elem(double x, float scale) { return oracle_e4m3_encode((double)((float)x / scale)); }
 
@@ -179,14 +197,14 @@ static uint8_t quant_elem(double x, float scale) { return oracle_e4m3_encode((do
  * Activation tiles 1 x 128 (ai.flicky.cc 3.3 item 2): row r, columns
  * [128g, 128g+128) share scale[r * G + g], G = cols / 128.
  */
-void oracle_quant_1x128(int64_t rows, int cols, const double* x, uint8_t* q, float* scale) {
+void oracle_quant_1x128(int64_t rows, int cols, const double* x, uint8_t* q, float* scale, int pow2) {
   const int G = cols / 128;
 #pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < rows; ++r)
     for (int g = 0; g < G; ++g) {
       double amax = 0.0;
       for (int c = 128 * g; c < 128 * g + 128; ++c) amax = fmax(amax, fabs(x[r * cols + c]));
-      float s = group_scale(amax);
+      float s = scale_of(amax, pow2);
       scale[r * G + g] = s;
       for (int c = 128 * g; c < 128 * g + 128; ++c) q[r * cols + c] = quant_elem(x[r * cols + c], s);
     }
@@ -196,7 +214,7 @@ void oracle_quant_1x128(int64_t rows, int cols, const double* x, uint8_t* q, flo
  * Weight blocks 128 x 128 (ai.flicky.cc 3.3 item 2): block (br, bc) of a
  * [rows, cols] matrix shares scale[br * (cols/128) + bc].
  */
-void oracle_quant_128x128(int64_t rows, int cols, const double* w, uint8_t* q, float* scale) {
+void oracle_quant_128x128(int64_t rows, int cols, const double* w, uint8_t* q, float* scale, int pow2) {
   const int64_t BR = rows / 128;
   const int BC = cols / 128;
 #pragma omp parallel for collapse(2) schedule(static)
@@ -205,7 +223,7 @@ void oracle_quant_128x128(int64_t rows, int cols, const double* w, uint8_t* q, f
       double amax = 0.0;
       for (int64_t r = 128 * br; r < 128 * br + 128; ++r)
         for (int c = 128 * bc; c < 128 * bc + 128; ++c) amax = fmax(amax, fabs(w[r * cols + c]));
-      float s = group_scale(amax);
+      float s = scale_of(amax, pow2);
       scale[br * BC + bc] = s;
       for (int64_t r = 128 * br; r < 128 * br + 128; ++r)
         for (int c = 128 * bc; c < 128 * bc + 128; ++c) q[r * cols + c] = quant_elem(w[r * cols + c], s);
@@ -217,6 +235,7 @@ void oracle_quant_128x128(int64_t rows, int cols, const double* w, uint8_t* q, f
  * matrices), on n rows:  y = W2 (SiLU(W1 x) * (W3 x)),  SiLU(a) = a sigmoid(a).
  * x [n, d], w1 and w3 [I, d], w2 [d, I] (nn.Linear layout), y [n, d]; fp64.
  * h_quant != 0: h is replaced by its FP8 1 x 128 quantise-dequantise along I
+ * (h_quant == 2: with UE8M0 scales)
  * before the down projection, as the FP8 scheme quantises the input of every
  * main GEMM (ai.flicky.cc 3.3 items 1-2).
  */
@@ -238,7 +257,7 @@ void oracle_swiglu(int64_t n, int d, int I, const double* x, const double* w1, c
       for (int gi = 0; gi < I / 128; ++gi) {
         double amax = 0.0;
         for (int i = 128 * gi; i < 128 * gi + 128; ++i) amax = fmax(amax, fabs(h[i]));
-        float s = group_scale(amax);
+        float s = scale_of(amax, h_quant == 2);
         for (int i = 128 * gi; i < 128 * gi + 128; ++i) h[i] = oracle_e4m3_decode(quant_elem(h[i], s)) * (double)s;
       }
     }

@@ -114,6 +114,16 @@ class LayerConfig:
     def rows(self) -> int:
         return self.T * self.k
 
+    @property
+    def is_fp8(self) -> bool:
+        """E4M3 expert GEMMs (amax/448 scales, or UE8M0 power-of-two scales)."""
+        return self.prec in ("fp8", "fp8_ue8m0")
+
+    @property
+    def oracle_fp8(self):
+        """The oracle's fp8 argument for this precision: False, True or "ue8m0"."""
+        return {"bf16": False, "fp8": True, "fp8_ue8m0": "ue8m0"}[self.prec]
+
 
 # (rho, alpha) of the clustered stream, chosen once with the oracle router so
 # that the 8192-token V3 batch has a max/mean expert load close to 4
@@ -162,6 +172,13 @@ CONFIGS = {
                               prec="fp8", rho=0.3, alpha=1.0),
     "tiny_fp8": LayerConfig("tiny_fp8", T=64, d=256, E=16, k=4, n_shared=1, inter=128,
                             prec="fp8", bias="zero", tokens="normal"),
+    # The FP8 scheme with UE8M0 (power-of-two) scales.
+    "tiny_ue8m0": LayerConfig("tiny_ue8m0", T=64, d=256, E=16, k=4, n_shared=1, inter=128,
+                              prec="fp8_ue8m0", bias="zero", tokens="normal"),
+    "ragged_ue8m0": LayerConfig("ragged_ue8m0", T=300, d=384, E=20, k=3, n_shared=1, inter=256,
+                                prec="fp8_ue8m0", rho=0.3, alpha=1.0),
+    "v3_ue8m0": LayerConfig("v3_ue8m0", T=8192, d=7168, E=256, k=8, n_shared=1, inter=2048,
+                            prec="fp8_ue8m0", rho=V3_RHO, alpha=V3_ALPHA),
 }
 
 

@@ -100,7 +100,7 @@ def test_calls_reject_null_and_small_workspace_without_a_gpu(lib):
     # bias update: k > E
     assert lib.moe_bias_update(4, 10, 5, fake, ctypes.c_float(0.001), fake, None) == 1
     # block quantiser: shape not a multiple of 128
-    assert lib.moe_quantize_fp8_blocks(fake, 100, 128, fake, fake, None) == 1
+    assert lib.moe_quantize_fp8_blocks(fake, 100, 128, fake, fake, 0, None) == 1
     # misaligned bf16 input
     assert lib.moe_combine(ctypes.byref(dm), fake + 2, fake, fake, fake, fake, fake, None) == 1
 

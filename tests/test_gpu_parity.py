@@ -69,14 +69,14 @@ def test_route_parity(name):
     assert (d[np.abs(d) > NEAR_TIE] < 0).all()
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "mid", "tiny_fp8", "ragged_fp8"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "mid", "tiny_fp8", "ragged_fp8", "ragged_ue8m0"])
 def test_permute_parity(name):
     cfg = synth.get_config(name)
     u, cent, bias = synth.tokens(cfg), synth.centroids(cfg), synth.bias(cfg)
     idx, _, _ = _route_gpu(cfg, u, cent, bias)
     dm, ws = _ws(cfg)
     R = cfg.T * cfg.k
-    fp8 = cfg.prec == "fp8"
+    fp8 = cfg.is_fp8
     offsets = torch.empty(cfg.E + 1, dtype=torch.int32, device=DEV)
     perm = torch.empty(R, dtype=torch.int32, device=DEV)
     slot = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=DEV)
@@ -92,20 +92,20 @@ def test_permute_parity(name):
     if not fp8:
         np.testing.assert_array_equal(x.view(torch.int16).cpu().numpy().view(np.uint16), ub[lay["perm"]])
     else:
-        q, s = oracle.quant_1x128(oracle.bf16_to_f64(ub))
+        q, s = oracle.quant_1x128(oracle.bf16_to_f64(ub), pow2=cfg.prec == "fp8_ue8m0")
         np.testing.assert_array_equal(x.cpu().numpy(), q[lay["perm"]])
         np.testing.assert_array_equal(xs.cpu().numpy().T, s[lay["perm"]])
 
 
-@pytest.mark.parametrize("prec", ["bf16", "fp8"])
-def test_quantize_blocks_bit_exact(prec):
+@pytest.mark.parametrize("pow2", [False, True])
+def test_quantize_blocks_bit_exact(pow2):
     w = synth.normal_bf16(synth.key(5, "w1", 3), (384, 512), 0.05)
     w[:128, :128] = 0                                      # all-zero block -> scale 1
     q = torch.empty((384, 512), dtype=torch.uint8, device=DEV)
     s = torch.empty((3, 4), dtype=torch.float32, device=DEV)
-    capi.moe_quantize_fp8_blocks(w.to(DEV), 384, 512, q, s)
+    capi.moe_quantize_fp8_blocks(w.to(DEV), 384, 512, q, s, pow2_scales=pow2)
     torch.cuda.synchronize()
-    rq, rs = oracle.quant_128x128(oracle.bf16_to_f64(synth.bf16_bits(w)))
+    rq, rs = oracle.quant_128x128(oracle.bf16_to_f64(synth.bf16_bits(w)), pow2=pow2)
     np.testing.assert_array_equal(q.cpu().numpy(), rq)
     np.testing.assert_array_equal(s.cpu().numpy(), rs)
     assert s[0, 0].item() == 1.0
@@ -160,7 +160,7 @@ def _forward_parity(cfg, sample=None, extra_chunks=True):
     return rel_err(h, h_ref), rel_err(y, y_ref)
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "tiny_fp8", "ragged_fp8"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "tiny_fp8", "ragged_fp8", "tiny_ue8m0", "ragged_ue8m0"])
 def test_forward_parity_full(name):
     cfg = synth.get_config(name)
     err, err_y = _forward_parity(cfg)
@@ -169,9 +169,10 @@ def test_forward_parity_full(name):
     assert err_y <= Y_TOL[cfg.prec]
 
 
-@pytest.mark.parametrize("name", ["mid", "mid_fp8", "mid_nodes"])
+@pytest.mark.parametrize("name", ["mid", "mid_fp8", "mid_nodes", "mid_ue8m0"])
 def test_forward_parity_mid_sampled(name):
-    extra = {"mid": {}, "mid_fp8": dict(prec="fp8"), "mid_nodes": dict(route_groups=8, route_group_limit=3)}
+    extra = {"mid": {}, "mid_fp8": dict(prec="fp8"), "mid_nodes": dict(route_groups=8, route_group_limit=3),
+             "mid_ue8m0": dict(prec="fp8_ue8m0")}
     cfg = synth.get_config("mid", **extra[name])
     sample = np.arange(0, cfg.T, 29)           # 142 tokens from every part of the batch, plus chunk cover
     err, err_y = _forward_parity(cfg, sample)

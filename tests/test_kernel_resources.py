@@ -25,7 +25,7 @@ from mixture_experts_layer_87_b300 import build as libbuild  # noqa: E402
 ENTRY = re.compile(r"Compiling entry function '(\w+)' for 'sm_103a'")
 SPILL = re.compile(r"(\d+) bytes spill stores, (\d+) bytes spill loads")
 REGS = re.compile(r"Used (\d+) registers")
-FP8 = re.compile(r"fp8_gemm_kernelILNS_3EpiE(\d)ELi(\d+)EE")
+FP8 = re.compile(r"fp8_gemm_kernelILNS_3EpiE(\d)ELi(\d+)ELb(\d)EE")
 
 
 @pytest.fixture(scope="module")
@@ -76,6 +76,7 @@ def test_fp8_gemm_register_split_matches_launch(ptxas_report):
         epi = (launch_regs * threads - 128 * ctrl) // (32 * ew) // 8 * 8
         assert 128 * ctrl + 32 * ew * epi <= launch_regs * threads
         assert launch_regs <= epi <= 256
-        seen.add((int(m.group(1)), ew))
-    # both epilogues (SwiGLU = 2, bf16 = 1) with 8 and 16 promotion warps
-    assert seen == {(1, 8), (1, 16), (2, 8), (2, 16)}, seen
+        seen.add((int(m.group(1)), ew, int(m.group(3))))
+    # both epilogues (SwiGLU = 2, bf16 = 1) with 8 and 16 promotion warps; the
+    # SwiGLU epilogue also with UE8M0 scales for h (last field 1)
+    assert seen == {(1, 8, 0), (1, 16, 0), (2, 8, 0), (2, 16, 0), (2, 8, 1), (2, 16, 1)}, seen

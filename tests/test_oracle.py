@@ -491,3 +491,59 @@ def test_node_limit_that_cannot_bind_changes_nothing():
         r = oracle.route(u, c, b, cfg.k, groups=groups, group_limit=limit)
         np.testing.assert_array_equal(r["idx"], free["idx"])
         np.testing.assert_array_equal(r["gate"], free["gate"])
+
+
+# ----------------------------------------------------------------------------
+# UE8M0 scales (ai.flicky.cc, continuation of 3.5: DeepSeek-V3.1's FP8 with
+# UE8M0 scales -- a scale is a bare power of two)
+def test_ue8m0_scales_are_the_next_power_of_two():
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((8, 512)) * np.exp2(rng.integers(-12, 12, (8, 1)))
+    x[3, :128] = 0.0
+    x[5, 128:256] = 0.0
+    x[5, 130] = 448.0 * 2.0 ** -3          # amax exactly 448 * 2^-3: the scale is 2^-3 itself
+    q, s = oracle.quant_1x128(x, pow2=True)
+    _, s_amax = oracle.quant_1x128(x)
+    m, e = np.frexp(s.astype(np.float64))
+    assert (m == 0.5).all()                                  # every scale a power of two
+    assert (s >= s_amax).all() and (s < 2 * s_amax).all()    # the smallest one >= amax/448
+    assert s[3, 0] == 1.0 and s[5, 1] == np.float32(2.0 ** -3)
+    assert (np.abs(oracle.e4m3_decode(q)) <= 448).all()
+    deq = oracle.dequant_1x128(q, s)
+    sc = np.repeat(s.astype(np.float64), 128, 1)
+    normal = np.abs(x) / sc >= 2.0 ** -6
+    assert (np.abs(x - deq)[normal] <= 2.0 ** -4 * np.abs(x)[normal] * (1 + 1e-6)).all()
+    w = rng.standard_normal((256, 384)) / 20
+    _, sw = oracle.quant_128x128(w, pow2=True)
+    assert (np.frexp(sw.astype(np.float64))[0] == 0.5).all()
+
+
+def test_ue8m0_quantisers_match_the_dense_statement():
+    rng = np.random.default_rng(32)
+    x = rng.standard_normal((6, 384)) * np.exp2(rng.integers(-8, 8, (6, 1)))
+    np.testing.assert_array_equal(oracle.fp8_roundtrip_1x128(x, pow2=True), brute.quant_dequant(x, 1, 128, True))
+    w = rng.standard_normal((256, 256)) * 0.03
+    np.testing.assert_array_equal(oracle.fp8_roundtrip_128x128(w, pow2=True), brute.quant_dequant(w, 128, 128, True))
+    # and the pow2 rule of the dense statement itself, on hand-picked values
+    np.testing.assert_array_equal(brute.pow2_at_least(np.array([1.0, 1.5, 0.25, 0.3, 3.0], np.float32)),
+                                  np.array([1.0, 2.0, 0.25, 0.5, 4.0], np.float32))
+
+
+@pytest.mark.parametrize("name", ["tiny_fp8", "ragged_fp8"])
+def test_ue8m0_layer_equals_dense_statement(name):
+    cfg = synth.get_config(name)
+    b = np.asarray(synth.normal_f32(4244, (cfg.E,), 0.02))
+    u, c, _, routed, shared = _tiny_layer(cfg)
+    r = oracle.route(synth.bf16_bits(u), synth.bf16_bits(c), b, cfg.k)
+    out = oracle.layer_output(synth.bf16_bits(u), np.arange(cfg.T), r["idx"], r["gate"],
+                              lambda e: _bits(routed[e]), lambda s: _bits(shared[s]), cfg.n_shared, cfg.E,
+                              fp8="ue8m0")
+    f = lambda ws: tuple(w.double().numpy() for w in ws)
+    dense = brute.dense_layer_fp8(u.double().numpy(), c.double().numpy(), b, cfg.k,
+                                  [f(w) for w in routed], [f(w) for w in shared], pow2=True)
+    scale = np.abs(dense["out"]).max()
+    np.testing.assert_allclose(out, dense["out"], rtol=0, atol=1e-12 * scale)
+    # a different quantisation from the amax/448 one (else the test says nothing)
+    other = oracle.layer_output(synth.bf16_bits(u), np.arange(cfg.T), r["idx"], r["gate"],
+                                lambda e: _bits(routed[e]), lambda s: _bits(shared[s]), cfg.n_shared, cfg.E, fp8=True)
+    assert np.abs(other - out).max() > 1e-6 * scale
