@@ -293,6 +293,60 @@ moe_status moe_forward_replicated(const moe_dims* dims, const moe_weights* w, co
                                   void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Backward pass of the layer (bf16 layers only; MOE_ERR_UNSUPPORTED for FP8).
+ * Given dL/dh' (dout), the gradients of the layer equation of ai.flicky.cc
+ * 2.1.2 (xyznot.com Method 2) with respect to its input u, the router
+ * centroids and every expert weight.  The selection is held fixed -- the
+ * gradient flows through the gate values g = s / sum s, not through the top-k
+ * choice -- and the bias, which the pages update by the sign rule
+ * (moe_bias_update), gets no gradient.  Weight and centroid gradients are
+ * fp32 (ai.flicky.cc 3.3 item 1: weight gradients are kept in higher
+ * precision); activations inside are bf16, as in the forward.
+ *
+ * The data-gradient products run on transposed weights, prepared once by
+ * moe_transpose_expert_weights:
+ *   w13t [n, d, 2I] = w13 [n, 2I, d] transposed per expert (the w13 row
+ *   interleave becomes the column order), w2t [n, I, d] = w2 [n, d, I]
+ *   transposed.  n = E for the routed experts, n_shared for the shared ones.
+ *
+ * moe_backward recomputes the forward's routing, dispatch and expert
+ * activations (the same kernels), then:
+ *   dy = g G (routed rows), dg = G . y, ds = (dg - sum g dg) / S,
+ *   dz = ds s (1 - s);  dh = dy W2;  da, db from the SwiGLU derivative;
+ *   dx = [da db] W13;  du = G + sum_j dx_j + sum_s dx_s + sum_j dz_j c_{e_j};
+ *   dW2 = dy^T h, dW13 = [da db]^T x per expert (fp32 GEMMs over the expert's
+ *   tokens), dcentroids_e = sum over its tokens of dz u.
+ *   dout   [T, d] bf16 dL/dh'.
+ *   grads  outputs, all fp32 device memory: du [T, d]; dcentroids [E, d];
+ *          dw13 [E, 2I, d] and dw2 [E, d, I] in the layout of w13 and w2 (an
+ *          expert no token chose gets zeros); dws13, dws2 the same for the
+ *          shared experts (unused when n_shared == 0).
+ *   ws     at least moe_backward_workspace_size bytes.
+ */
+typedef struct {
+  const void* w13t;   /* [E, d, 2I] bf16 */
+  const void* w2t;    /* [E, I, d] bf16 */
+  const void* ws13t;  /* [n_shared, d, 2I] bf16 */
+  const void* ws2t;   /* [n_shared, I, d] bf16 */
+} moe_weights_t;
+
+typedef struct {
+  float* du;
+  float* dcentroids;
+  float* dw13;
+  float* dw2;
+  float* dws13;
+  float* dws2;
+} moe_grads;
+
+moe_status moe_backward_workspace_size(const moe_dims* dims, size_t* bytes);
+moe_status moe_transpose_expert_weights(int32_t n_experts, int32_t inter, int32_t d, const uint16_t* w13,
+                                        const uint16_t* w2, uint16_t* w13t, uint16_t* w2t, void* stream);
+moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_weights_t* wt, const uint16_t* u,
+                        const float* bias, const uint16_t* dout, const moe_grads* grads, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/*
  * moe_forward with stage timing.  `events` holds n_events >= MOE_PROFILE_EVENTS
  * cudaEvent_t handles (passed as void*) created by the caller; the call
  * records events[0] on `stream` before its first kernel and events[i] after

@@ -24,7 +24,8 @@ MOE_BF16, MOE_FP8_E4M3, MOE_FP8_UE8M0 = 0, 1, 2
 EXPORTS = (
     "moe_status_string", "moe_workspace_size", "moe_route", "moe_route_noalloc", "moe_permute", "moe_grouped_ffn",
     "moe_combine", "moe_bias_update", "moe_forward", "moe_forward_profiled", "moe_forward_replicated",
-    "moe_plan_replicas", "moe_pack_gate_up",
+    "moe_plan_replicas", "moe_backward", "moe_backward_workspace_size", "moe_transpose_expert_weights",
+    "moe_pack_gate_up",
     "moe_quantize_fp8_blocks",
     "moe_read_device_status", "moe_selftest_wait_timeout",
 )
@@ -40,6 +41,16 @@ class moe_dims(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("n_shared", ctypes.c_int32), ("inter", ctypes.c_int32), ("prec", ctypes.c_int32),
                 ("route_groups", ctypes.c_int32), ("route_group_limit", ctypes.c_int32)]
+
+
+class moe_weights_t(ctypes.Structure):
+    _fields_ = [("w13t", ctypes.c_void_p), ("w2t", ctypes.c_void_p), ("ws13t", ctypes.c_void_p),
+                ("ws2t", ctypes.c_void_p)]
+
+
+class moe_grads(ctypes.Structure):
+    _fields_ = [("du", ctypes.c_void_p), ("dcentroids", ctypes.c_void_p), ("dw13", ctypes.c_void_p),
+                ("dw2", ctypes.c_void_p), ("dws13", ctypes.c_void_p), ("dws2", ctypes.c_void_p)]
 
 
 class moe_weights(ctypes.Structure):
@@ -76,6 +87,10 @@ def lib() -> ctypes.CDLL:
             "moe_forward_replicated": ([D, ctypes.POINTER(moe_weights), vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp],
                                        ctypes.c_int),
             "moe_plan_replicas": ([i32, vp, i32, vp, vp, vp], ctypes.c_int),
+            "moe_backward_workspace_size": ([D, ctypes.POINTER(sz)], ctypes.c_int),
+            "moe_transpose_expert_weights": ([i32, i32, i32, vp, vp, vp, vp, vp], ctypes.c_int),
+            "moe_backward": ([D, ctypes.POINTER(moe_weights), ctypes.POINTER(moe_weights_t), vp, vp, vp,
+                              ctypes.POINTER(moe_grads), vp, sz, vp], ctypes.c_int),
             "moe_pack_gate_up": ([vp, vp, i32, i32, i32, vp, vp], ctypes.c_int),
             "moe_quantize_fp8_blocks": ([vp, i64, i32, vp, vp, i32, vp], ctypes.c_int),
             "moe_read_device_status": ([vp, vp], ctypes.c_int),
@@ -234,3 +249,20 @@ def moe_read_device_status(ws, stream=None) -> int:
 def moe_selftest_wait_timeout(ws, timeout_us, stream=None):
     _check(lib().moe_selftest_wait_timeout(_ptr(ws), ws.numel() * ws.element_size(), int(timeout_us),
                                            _stream(stream)), "moe_selftest_wait_timeout")
+
+
+def moe_backward_workspace_size(dm: moe_dims) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_backward_workspace_size(ctypes.byref(dm), ctypes.byref(n)), "moe_backward_workspace_size")
+    return n.value
+
+
+def moe_transpose_expert_weights(n_experts, inter, d, w13, w2, w13t, w2t, stream=None):
+    _check(lib().moe_transpose_expert_weights(int(n_experts), int(inter), int(d), _ptr(w13), _ptr(w2), _ptr(w13t),
+                                              _ptr(w2t), _stream(stream)), "moe_transpose_expert_weights")
+
+
+def moe_backward(dm, weights: moe_weights, weights_t: moe_weights_t, u, bias, dout, grads: moe_grads, ws, stream=None):
+    _check(lib().moe_backward(ctypes.byref(dm), ctypes.byref(weights), ctypes.byref(weights_t), _ptr(u), _ptr(bias),
+                              _ptr(dout), ctypes.byref(grads), _ptr(ws), ws.numel() * ws.element_size(),
+                              _stream(stream)), "moe_backward")

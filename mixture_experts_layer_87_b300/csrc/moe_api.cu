@@ -15,8 +15,10 @@
 
 #include "expert_gemm.cuh"
 #include "fp8_gemm.cuh"
+#include "backward.cuh"
 #include "kernels.cuh"
 #include "moe.h"
+#include "wgrad_gemm.cuh"
 
 using namespace moe;
 
@@ -716,6 +718,140 @@ moe_status forward_impl(const moe_dims* dims, const moe_weights* w, const uint16
 
 }  // namespace
 
+// =================================================================== backward (bf16)
+namespace {
+
+// Backward workspace: the forward's layout (routing, dispatch, x_perm, h, y)
+// followed by the backward's own buffers.
+struct BwdLayout {
+  Layout f;
+  size_t queue, ab, dy, dh, dab, dx, dz_row, ab_s, dh_s, dab_s, dx_s, pad_off, col_of_row, wg_r, wg_s2, wg_s13;
+  size_t xT, dyT, hT, dabT, uT, GT, hsT, dabsT, total;
+  int64_t Rp, Tp;
+};
+
+BwdLayout make_bwd_layout(const moe_dims& d) {
+  BwdLayout B{};
+  B.f = make_layout(d);
+  size_t off = B.f.total;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align_up(bytes > 0 ? bytes : 1);
+    return o;
+  };
+  const int64_t T = d.T, R = T * d.k, E = d.E, I = d.inter, D = d.d, Ns = d.n_shared;
+  B.Rp = (R + 64 * E + 63) / 64 * 64;  // every expert's rows padded to a multiple of 64 columns
+  B.Tp = (T + 63) / 64 * 64;
+  B.queue = take(16 * sizeof(int));
+  B.ab = take(R * 2 * I * 2);
+  B.dy = take(R * D * 2);
+  B.dh = take(R * I * 2);
+  B.dab = take(R * 2 * I * 2);
+  B.dx = take(R * D * 2);
+  B.dz_row = take(R * 4);
+  B.ab_s = take(Ns * T * 2 * I * 2);
+  B.dh_s = take(Ns * T * I * 2);
+  B.dab_s = take(Ns * T * 2 * I * 2);
+  B.dx_s = take(Ns * T * D * 2);
+  B.pad_off = take((E + 2) * 4);
+  B.col_of_row = take(R * 4);
+  B.wg_r = take(E * sizeof(WgradGroup));
+  B.wg_s2 = take((Ns + 1) * sizeof(WgradGroup));
+  B.wg_s13 = take((Ns + 1) * sizeof(WgradGroup));
+  B.xT = take(D * B.Rp * 2);
+  B.dyT = take(D * B.Rp * 2);
+  B.hT = take(I * B.Rp * 2);
+  B.dabT = take(2 * I * B.Rp * 2);
+  B.uT = take(D * B.Tp * 2);
+  B.GT = take(D * B.Tp * 2);
+  B.hsT = take(I * Ns * B.Tp * 2);
+  B.dabsT = take(2 * I * Ns * B.Tp * 2);
+  B.total = off;
+  return B;
+}
+
+// WgradGroup table of the routed experts from the padded offsets: the same
+// K range in A and B.
+__global__ void wgrad_table_kernel(const int32_t* __restrict__ pad_off, int G, WgradGroup* __restrict__ out) {
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g < G) out[g] = WgradGroup{pad_off[g], pad_off[g], pad_off[g + 1] - pad_off[g], 0};
+}
+
+// WgradGroup table of the shared experts: group s reads K columns
+// [s * a_step, + len) of A and [s * b_step, + len) of B.
+__global__ void wgrad_strided_table_kernel(int G, int a_step, int b_step, int len, WgradGroup* __restrict__ out) {
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g < G) out[g] = WgradGroup{g * a_step, g * b_step, len, 0};
+}
+
+// One bf16 expert-GEMM launch (BF16 epilogue): out[rows of group g] = X[rows] . W_g^T.
+//   table != nullptr: groups from the device table (chunk totals in mt_total,
+//   chunk -> group in cgroup); else n_groups uniform groups of uni_m rows,
+//   X rows of group g starting at g * uni_a_step, output rows at g * uni_m.
+moe_status xgemm_bf16(const void* w, int64_t w_rows, int Nw, int K, const void* x, int64_t x_rows, void* out,
+                      int64_t out_ld, int n_groups, const GroupEntry* table, const int32_t* mt_total,
+                      const int32_t* cgroup, int64_t chunks_bound, int uni_m, int uni_a_step, int* queue, int* status,
+                      cudaStream_t st) {
+  CUtensorMap tw, tx;
+  MOE_TRY(make_tmap(&tw, w, false, w_rows, K, 256));
+  MOE_TRY(make_tmap(&tx, x, false, x_rows, K, kChunkBf16));
+  XGemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.status = status;
+  a.queue = queue;
+  a.groups = table;
+  a.ch_total = mt_total;
+  a.chunk_group = cgroup;
+  a.n_groups = n_groups;
+  a.uni_m = uni_m;
+  a.uni_a_step = uni_a_step;
+  a.uni_out_step = uni_m;
+  a.Nw = Nw;
+  a.K = K;
+  a.x_rows = static_cast<int32_t>(x_rows);
+  a.out = out;
+  a.out_ld = out_ld;
+#ifdef MOE_CHECK
+  a.w_rows = w_rows;
+  a.out_rows = static_cast<int32_t>(table ? x_rows : int64_t(uni_m) * n_groups);
+#endif
+  const int64_t chunks = table ? chunks_bound : int64_t(n_groups) * cdiv(uni_m, kChunkBf16);
+  return launch_xgemm<Epi::BF16>(tw, tx, a, chunks * cdiv(Nw, 256), st);
+}
+
+// Transposed copy src [batch][rows][C] -> dst: dst + b * dst_batch + c * ldd + col(r).
+moe_status transpose_bf16(const void* src, int rows, int C, int64_t src_batch, const int32_t* col_of_row, void* dst,
+                          int64_t ldd, int64_t dst_batch, int batch, cudaStream_t st) {
+  if (rows <= 0 || C <= 0 || batch <= 0) return MOE_OK;
+  dim3 grid(static_cast<unsigned>(cdiv(C, 32)), static_cast<unsigned>(cdiv(rows, 32)), static_cast<unsigned>(batch));
+  transpose_bf16_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, C, src_batch, col_of_row,
+                                               static_cast<__nv_bfloat16*>(dst), ldd, dst_batch);
+  return launched();
+}
+
+// Weight gradients of n_groups groups: out[g] [M, N] fp32 = A[:, ka..] . B[:, kb..]^T.
+moe_status wgrad(const void* A, int64_t a_cols, int M, const void* Bm, int64_t b_cols, int N,
+                 const WgradGroup* table, int n_groups, float* out, int* status, cudaStream_t st) {
+  if (n_groups <= 0) return MOE_OK;
+  CUtensorMap ta, tb;
+  MOE_TRY(make_tmap(&ta, A, false, M, a_cols, 128));
+  MOE_TRY(make_tmap(&tb, Bm, false, N, b_cols, 256));
+  WgradArgs a{table, M, N, out, status};
+  constexpr size_t smem = wgrad_smem_bytes();
+  MOE_TRY(cuda_ok(cudaFuncSetAttribute(wgrad_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem))));
+  dim3 grid(static_cast<unsigned>(cdiv(N, 256)), static_cast<unsigned>(M / 128), static_cast<unsigned>(n_groups));
+  wgrad_gemm_kernel<<<grid, 192, smem, st>>>(ta, tb, a);
+  return launched();
+}
+
+unsigned ew_blocks(int64_t n) {  // grid of the elementwise kernels (grid-strided)
+  const int64_t b = cdiv(n, 256);
+  return static_cast<unsigned>(b < 148 * 16 ? (b > 0 ? b : 1) : 148 * 16);
+}
+
+}  // namespace
+
 extern "C" {
 
 moe_status moe_forward_profiled(const moe_dims* dims, const moe_weights* w, const uint16_t* u, const float* bias,
@@ -759,6 +895,182 @@ moe_status moe_forward_replicated(const moe_dims* dims, const moe_weights* w, co
     return MOE_ERR_INVALID_ARG;
   const ReplicaPlan rp{replica_first, replica_count, slot_expert, n_slots};
   return forward_impl(dims, w, u, bias, out, counts_out, ws, ws_bytes, stream, nullptr, 0, &rp);
+}
+
+moe_status moe_backward_workspace_size(const moe_dims* dims, size_t* bytes) {
+  MOE_TRY(check_dims(dims));
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  if (dims->prec != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  *bytes = make_bwd_layout(*dims).total;
+  return MOE_OK;
+}
+
+moe_status moe_transpose_expert_weights(int32_t n_experts, int32_t inter, int32_t d, const uint16_t* w13,
+                                        const uint16_t* w2, uint16_t* w13t, uint16_t* w2t, void* stream) {
+  if (n_experts <= 0 || n_experts > 65535 || inter <= 0 || d <= 0 || inter % 128 || d % 128) return MOE_ERR_INVALID_ARG;
+  if (!w13 || !w2 || !w13t || !w2t) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t I2 = 2 * int64_t(inter);
+  MOE_TRY(transpose_bf16(w13, static_cast<int>(I2), d, I2 * d, nullptr, w13t, I2, I2 * d, n_experts, st));
+  return transpose_bf16(w2, d, inter, int64_t(d) * inter, nullptr, w2t, d, int64_t(d) * inter, n_experts, st);
+}
+
+moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_weights_t* wt, const uint16_t* u,
+                        const float* bias, const uint16_t* dout, const moe_grads* gr, void* ws, size_t ws_bytes,
+                        void* stream) {
+  MOE_TRY(check_dims(dims));
+  if (dims->prec != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  MOE_TRY(check_weights(*dims, w));
+  const moe_dims& d = *dims;
+  if (!wt || !wt->w13t || !wt->w2t || (d.n_shared > 0 && (!wt->ws13t || !wt->ws2t))) return MOE_ERR_INVALID_ARG;
+  if (!gr || !gr->du || !gr->dcentroids || !gr->dw13 || !gr->dw2 || (d.n_shared > 0 && (!gr->dws13 || !gr->dws2)))
+    return MOE_ERR_INVALID_ARG;
+  if (!bias || (d.T > 0 && (!u || !dout)) || !aligned16(u) || !aligned16(dout)) return MOE_ERR_INVALID_ARG;
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return MOE_ERR_INVALID_ARG;
+  const BwdLayout B = make_bwd_layout(d);
+  if (ws_bytes < B.total) return MOE_ERR_WORKSPACE;
+  const Layout& L = B.f;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t T = d.T, R = T * d.k, E = d.E, I = d.inter, D = d.d, Ns = d.n_shared, I2 = 2 * I;
+  int* status = at<int>(ws, L.status);
+  int* queue = at<int>(ws, B.queue);
+  MOE_TRY(cuda_ok(cudaMemsetAsync(status, 0, sizeof(int), st)));
+  MOE_TRY(cuda_ok(cudaMemsetAsync(queue, 0, 16 * sizeof(int), st)));
+  if (T == 0) {  // no tokens: zero gradients
+    MOE_TRY(cuda_ok(cudaMemsetAsync(gr->dcentroids, 0, E * D * 4, st)));
+    MOE_TRY(cuda_ok(cudaMemsetAsync(gr->dw13, 0, E * I2 * D * 4, st)));
+    MOE_TRY(cuda_ok(cudaMemsetAsync(gr->dw2, 0, E * D * I * 4, st)));
+    if (Ns > 0) {
+      MOE_TRY(cuda_ok(cudaMemsetAsync(gr->dws13, 0, Ns * I2 * D * 4, st)));
+      MOE_TRY(cuda_ok(cudaMemsetAsync(gr->dws2, 0, Ns * D * I * 4, st)));
+    }
+    return MOE_OK;
+  }
+  const int W = static_cast<int>((T + 31) / 32);
+  uint32_t* mask = at<uint32_t>(ws, L.mask);
+  MOE_TRY(cuda_ok(cudaMemsetAsync(mask, 0, sizeof(uint32_t) * size_t(E) * W, st)));
+  // --- the forward's routing and dispatch, recomputed
+  int32_t* idx = at<int32_t>(ws, L.idx);
+  float* gate = at<float>(ws, L.gate);
+  float* z = at<float>(ws, L.z);
+  MOE_TRY(enqueue_route(d, u, w->centroids, bias, idx, gate, at<int32_t>(ws, L.counts), mask, z, status, st));
+  GroupEntry* groups = at<GroupEntry>(ws, L.groups);
+  int32_t* mt_total = at<int32_t>(ws, L.mt_total);
+  int32_t* cgroup = at<int32_t>(ws, L.cgroup);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* perm = at<int32_t>(ws, L.perm);
+  int32_t* slot = at<int32_t>(ws, L.slot);
+  void* x = at<void>(ws, L.x);
+  MOE_TRY(enqueue_dispatch(d, idx, u, mask, at<int32_t>(ws, L.wprefix), at<int32_t>(ws, L.cnt), offsets, groups,
+                           mt_total, cgroup, perm, slot, x, nullptr, nullptr, nullptr, status, st));
+  const int64_t chunks = cdiv(R + int64_t(kChunkBf16 - 1) * E, kChunkBf16);
+  void* ab = at<void>(ws, B.ab);
+  void* h = at<void>(ws, L.h);
+  void* y = at<void>(ws, L.y);
+  // --- routed experts: a, b (gate/up pre-activations), h, y
+  MOE_TRY(xgemm_bf16(w->w13, E * I2, static_cast<int>(I2), static_cast<int>(D), x, R, ab, I2, static_cast<int>(E),
+                     groups, mt_total, cgroup, chunks, 0, 0, queue + 0, status, st));
+  swiglu_fwd_kernel<<<ew_blocks(R * I), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab), R, static_cast<int>(I),
+                                                       static_cast<__nv_bfloat16*>(h));
+  MOE_TRY(launched());
+  MOE_TRY(xgemm_bf16(w->w2, E * D, static_cast<int>(D), static_cast<int>(I), h, R, y, D, static_cast<int>(E), groups,
+                     mt_total, cgroup, chunks, 0, 0, queue + 1, status, st));
+  // --- combine and gates backward: dy, dz, du = G + router share
+  void* dy = at<void>(ws, B.dy);
+  float* dz_row = at<float>(ws, B.dz_row);
+  const LogitsSplit sp = logits_split(d);
+  combine_bwd_kernel<<<static_cast<unsigned>(T), 128, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(y), slot, idx, gate, z,
+      sp.splits, T * E, reinterpret_cast<const __nv_bfloat16*>(w->centroids), static_cast<int>(T), static_cast<int>(D),
+      d.k, static_cast<int>(E), R, static_cast<__nv_bfloat16*>(dy), dz_row, gr->du, status);
+  MOE_TRY(launched());
+  // --- data gradients of the routed experts
+  void* dh = at<void>(ws, B.dh);
+  void* dab = at<void>(ws, B.dab);
+  void* dx = at<void>(ws, B.dx);
+  MOE_TRY(xgemm_bf16(wt->w2t, E * I, static_cast<int>(I), static_cast<int>(D), dy, R, dh, I, static_cast<int>(E), groups,
+                     mt_total, cgroup, chunks, 0, 0, queue + 2, status, st));
+  swiglu_bwd_kernel<<<ew_blocks(R * I), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab),
+                                                       static_cast<const __nv_bfloat16*>(dh), R, static_cast<int>(I),
+                                                       static_cast<__nv_bfloat16*>(dab));
+  MOE_TRY(launched());
+  MOE_TRY(xgemm_bf16(wt->w13t, E * D, static_cast<int>(D), static_cast<int>(I2), dab, R, dx, D, static_cast<int>(E),
+                     groups, mt_total, cgroup, chunks, 0, 0, queue + 3, status, st));
+  // --- shared experts: every token, the output gradient is G itself
+  void* ab_s = at<void>(ws, B.ab_s);
+  void* h_s = at<void>(ws, L.hsh);
+  void* dh_s = at<void>(ws, B.dh_s);
+  void* dab_s = at<void>(ws, B.dab_s);
+  void* dx_s = at<void>(ws, B.dx_s);
+  if (Ns > 0) {
+    const int Ti = static_cast<int>(T), Nsi = static_cast<int>(Ns);
+    MOE_TRY(xgemm_bf16(w->ws13, Ns * I2, static_cast<int>(I2), static_cast<int>(D), u, T, ab_s, I2, Nsi, nullptr,
+                       nullptr, nullptr, 0, Ti, 0, queue + 4, status, st));
+    swiglu_fwd_kernel<<<ew_blocks(Ns * T * I), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab_s), Ns * T,
+                                                              static_cast<int>(I), static_cast<__nv_bfloat16*>(h_s));
+    MOE_TRY(launched());
+    MOE_TRY(xgemm_bf16(wt->ws2t, Ns * I, static_cast<int>(I), static_cast<int>(D), dout, T, dh_s, I, Nsi, nullptr,
+                       nullptr, nullptr, 0, Ti, 0, queue + 5, status, st));
+    swiglu_bwd_kernel<<<ew_blocks(Ns * T * I), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab_s),
+                                                              static_cast<const __nv_bfloat16*>(dh_s), Ns * T,
+                                                              static_cast<int>(I), static_cast<__nv_bfloat16*>(dab_s));
+    MOE_TRY(launched());
+    MOE_TRY(xgemm_bf16(wt->ws13t, Ns * D, static_cast<int>(D), static_cast<int>(I2), dab_s, Ns * T, dx_s, D, Nsi,
+                       nullptr, nullptr, nullptr, 0, Ti, Ti, queue + 6, status, st));
+  }
+  gather_dx_kernel<<<static_cast<unsigned>(T), 128, 0, st>>>(static_cast<const __nv_bfloat16*>(dx), slot, d.k, R,
+                                                              static_cast<const __nv_bfloat16*>(dx_s),
+                                                              static_cast<int>(Ns), static_cast<int>(T),
+                                                              static_cast<int>(D), gr->du);
+  MOE_TRY(launched());
+  // --- centroid gradient
+  dcent_kernel<<<dim3(static_cast<unsigned>(E), static_cast<unsigned>(cdiv(D, 256))), 256, 0, st>>>(
+      dz_row, perm, offsets, reinterpret_cast<const __nv_bfloat16*>(u), static_cast<int>(D), gr->dcentroids);
+  MOE_TRY(launched());
+  // --- weight gradients of the routed experts: the expert's tokens along K
+  int32_t* pad_off = at<int32_t>(ws, B.pad_off);
+  int32_t* col_of_row = at<int32_t>(ws, B.col_of_row);
+  WgradGroup* wg_r = at<WgradGroup>(ws, B.wg_r);
+  pad_plan_kernel<<<1, 1024, 0, st>>>(offsets, static_cast<int>(E), static_cast<int>(R), pad_off, col_of_row, status);
+  MOE_TRY(launched());
+  wgrad_table_kernel<<<static_cast<unsigned>(cdiv(E, 256)), 256, 0, st>>>(pad_off, static_cast<int>(E), wg_r);
+  MOE_TRY(launched());
+  void* xT = at<void>(ws, B.xT);
+  void* dyT = at<void>(ws, B.dyT);
+  void* hT = at<void>(ws, B.hT);
+  void* dabT = at<void>(ws, B.dabT);
+  MOE_TRY(cuda_ok(cudaMemsetAsync(xT, 0, B.dabT + 2 * I2 * B.Rp - B.xT, st)));  // xT .. dabT: the zero padding
+  MOE_TRY(transpose_bf16(x, static_cast<int>(R), static_cast<int>(D), 0, col_of_row, xT, B.Rp, 0, 1, st));
+  MOE_TRY(transpose_bf16(dy, static_cast<int>(R), static_cast<int>(D), 0, col_of_row, dyT, B.Rp, 0, 1, st));
+  MOE_TRY(transpose_bf16(h, static_cast<int>(R), static_cast<int>(I), 0, col_of_row, hT, B.Rp, 0, 1, st));
+  MOE_TRY(transpose_bf16(dab, static_cast<int>(R), static_cast<int>(I2), 0, col_of_row, dabT, B.Rp, 0, 1, st));
+  MOE_TRY(wgrad(dyT, B.Rp, static_cast<int>(D), hT, B.Rp, static_cast<int>(I), wg_r, static_cast<int>(E), gr->dw2,
+                status, st));
+  MOE_TRY(wgrad(dabT, B.Rp, static_cast<int>(I2), xT, B.Rp, static_cast<int>(D), wg_r, static_cast<int>(E), gr->dw13,
+                status, st));
+  // --- weight gradients of the shared experts (K = all tokens, padded)
+  if (Ns > 0) {
+    void* uT = at<void>(ws, B.uT);
+    void* GT = at<void>(ws, B.GT);
+    void* hsT = at<void>(ws, B.hsT);
+    void* dabsT = at<void>(ws, B.dabsT);
+    const int Tp = static_cast<int>(B.Tp), Ti = static_cast<int>(T), Nsi = static_cast<int>(Ns);
+    MOE_TRY(cuda_ok(cudaMemsetAsync(uT, 0, B.dabsT + 2 * I2 * Ns * B.Tp - B.uT, st)));
+    MOE_TRY(transpose_bf16(u, Ti, static_cast<int>(D), 0, nullptr, uT, Tp, 0, 1, st));
+    MOE_TRY(transpose_bf16(dout, Ti, static_cast<int>(D), 0, nullptr, GT, Tp, 0, 1, st));
+    MOE_TRY(transpose_bf16(h_s, Ti, static_cast<int>(I), T * I, nullptr, hsT, Ns * Tp, Tp, Nsi, st));
+    MOE_TRY(transpose_bf16(dab_s, Ti, static_cast<int>(I2), T * I2, nullptr, dabsT, Ns * Tp, Tp, Nsi, st));
+    WgradGroup* wg_s2 = at<WgradGroup>(ws, B.wg_s2);
+    WgradGroup* wg_s13 = at<WgradGroup>(ws, B.wg_s13);
+    wgrad_strided_table_kernel<<<1, 256, 0, st>>>(Nsi, 0, Tp, Tp, wg_s2);       // A = G^T, B = h_s^T
+    MOE_TRY(launched());
+    wgrad_strided_table_kernel<<<1, 256, 0, st>>>(Nsi, Tp, 0, Tp, wg_s13);      // A = dab_s^T, B = u^T
+    MOE_TRY(launched());
+    MOE_TRY(wgrad(GT, Tp, static_cast<int>(D), hsT, Ns * Tp, static_cast<int>(I), wg_s2, Nsi, gr->dws2, status, st));
+    MOE_TRY(wgrad(dabsT, Ns * Tp, static_cast<int>(I2), uT, Tp, static_cast<int>(D), wg_s13, Nsi, gr->dws13, status,
+                  st));
+  }
+  return MOE_OK;
 }
 
 moe_status moe_pack_gate_up(const uint16_t* w1, const uint16_t* w3, int32_t E, int32_t inter, int32_t d,

@@ -100,6 +100,41 @@ class MoELayer:
     def status(self) -> int:
         return capi.moe_read_device_status(self.ws)
 
+    # ------------------------------------------------------------ backward (bf16)
+    def prepare_backward(self) -> None:
+        """Transposed copies of the expert weights and the backward workspace."""
+        assert not self.fp8, "the backward pass is built for bf16 layers"
+        dev, I, d = self.device, self.inter, self.d
+        ns = max(self.n_shared, 1)
+        self.w13t = torch.empty((self.E, d, 2 * I), dtype=torch.bfloat16, device=dev)
+        self.w2t = torch.empty((self.E, I, d), dtype=torch.bfloat16, device=dev)
+        self.ws13t = torch.empty((ns, d, 2 * I), dtype=torch.bfloat16, device=dev)
+        self.ws2t = torch.empty((ns, I, d), dtype=torch.bfloat16, device=dev)
+        capi.moe_transpose_expert_weights(self.E, I, d, self.w13, self.w2, self.w13t, self.w2t)
+        if self.n_shared:
+            capi.moe_transpose_expert_weights(self.n_shared, I, d, self.ws13, self.ws2, self.ws13t, self.ws2t)
+        self.ws_bwd = torch.empty(capi.moe_backward_workspace_size(self.dims), dtype=torch.uint8, device=dev)
+
+    def backward(self, u: torch.Tensor, bias: torch.Tensor, dout: torch.Tensor, stream=None) -> dict:
+        """Gradients (fp32) of the layer for dL/dh' = dout: du, dcentroids,
+        dw13/dw2 (routed, in the w13/w2 layouts) and dws13/dws2 (shared)."""
+        if not hasattr(self, "ws_bwd"):
+            self.prepare_backward()
+        dev, I, d, f = self.device, self.inter, self.d, torch.float32
+        ns = max(self.n_shared, 1)
+        g = dict(du=torch.empty((self.T, d), dtype=f, device=dev), dcentroids=torch.empty((self.E, d), dtype=f, device=dev),
+                 dw13=torch.empty((self.E, 2 * I, d), dtype=f, device=dev),
+                 dw2=torch.empty((self.E, d, I), dtype=f, device=dev),
+                 dws13=torch.empty((ns, 2 * I, d), dtype=f, device=dev),
+                 dws2=torch.empty((ns, d, I), dtype=f, device=dev))
+        wt = capi.moe_weights_t(self.w13t.data_ptr(), self.w2t.data_ptr(), self.ws13t.data_ptr(), self.ws2t.data_ptr())
+        gr = capi.moe_grads(*(g[k].data_ptr() for k in ("du", "dcentroids", "dw13", "dw2", "dws13", "dws2")))
+        capi.moe_backward(self.dims, self.weights(), wt, u, bias, dout, gr, self.ws_bwd, stream)
+        return g
+
+    def backward_status(self) -> int:
+        return capi.moe_read_device_status(self.ws_bwd)
+
 
 class HostPipeline:
     """The layer over batches that live in pinned host memory.

@@ -121,3 +121,17 @@ def test_range_checked_build_exports_the_same_symbols():
         assert hasattr(L, n), n
     L.moe_status_string.restype = ctypes.c_char_p
     assert b"range-checked" in L.moe_status_string(7)
+
+
+def test_backward_rejects_fp8_and_null_arguments(lib):
+    n = ctypes.c_size_t(0)
+    d8 = _dims(prec="fp8")
+    assert lib.moe_backward_workspace_size(ctypes.byref(d8), ctypes.byref(n)) == 2     # bf16 only
+    dm = _dims()
+    need = capi.moe_backward_workspace_size(dm)
+    assert need > capi.moe_workspace_size(dm)
+    fake = 1 << 20
+    w, wt, gr = capi.moe_weights(), capi.moe_weights_t(), capi.moe_grads()
+    assert lib.moe_backward(ctypes.byref(dm), ctypes.byref(w), ctypes.byref(wt), fake, fake, fake, ctypes.byref(gr),
+                            fake, need, None) == 1
+    assert lib.moe_transpose_expert_weights(2, 100, 128, fake, fake, fake, fake, None) == 1       # I % 128
