@@ -2,11 +2,18 @@
 oracle (oracle/backward.py, itself pinned to autograd and finite differences),
 with the GPU's own selection held fixed on both sides.
 
-Tolerance: max|err| / rms(ref) <= 5e-2 on every gradient.  The pass keeps its
-activations in bf16 as the forward does (a, b, h, y, dy, dh, da/db, dx: each
-rounded to 8 significant bits, 2^-9 relative), and a data gradient goes
-through up to four of those roundings; at the largest elements (max/rms ~ 5)
-that is a few percent.  Weight gradients sum over tokens in fp32."""
+Tolerances.  The pass keeps its activations in bf16 as the forward does (a,
+b, h, y, dy, dh, da/db, dx: each rounded to 8 significant bits, 2^-9
+relative), and a gradient goes through up to four of those roundings:
+  * data gradients (du, dcentroids): max|err| / rms(ref) <= 5e-2 -- a few
+    roundings at the largest elements (max/rms ~ 5);
+  * weight gradients: ||err|| / ||ref|| (Frobenius) <= 2e-2.  Their elements
+    are sums over an expert's few tokens of products of two activations, so
+    their distribution is heavy-tailed and max|err|/rms measures the tail, not
+    the arithmetic; four roundings of 2^-9/sqrt(3) rms each give ~0.5% in norm.
+  * and the arithmetic itself: dW2 of the first experts against the same
+    product replayed from the bf16-rounded a, b, h and dy (fp64):
+    ||err|| / ||ref|| <= 1e-3 (the GPU accumulates in fp32)."""
 import numpy as np
 import pytest
 import torch
@@ -19,7 +26,17 @@ from parity import HostLayer, rel_err
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-BWD_TOL = 5e-2
+BWD_TOL = 5e-2      # data gradients, max|err| / rms(ref)
+WG_TOL = 2e-2       # weight gradients, relative Frobenius norm
+REPLAY_TOL = 1e-3   # dW2 against the bf16-operand replay, relative Frobenius norm
+
+
+def fro_err(got, ref):
+    return float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+
+
+def _bf16(a):
+    return torch.from_numpy(np.asarray(a, np.float64)).float().to(torch.bfloat16).double().numpy()
 
 
 @pytest.mark.parametrize("name", ["tiny", "ragged", "mid"])
@@ -42,21 +59,35 @@ def test_backward_matches_oracle(name):
                             cfg.n_shared, cfg.E)
     got = {k: v.cpu().numpy().astype(np.float64) for k, v in g.items()}
     errs = {"du": rel_err(got["du"], ref["du"]), "dcentroids": rel_err(got["dcentroids"], ref["dcent"])}
+    print(f"{name}: du {errs['du']:.3e}, dcentroids {errs['dcentroids']:.3e} (max|err|/rms)")
+    assert all(v <= BWD_TOL for v in errs.values()), errs
     I = cfg.inter
+    werr = {}
     for e, (dw1, dw3, dw2) in ref["dw_routed"].items():
         # w13 interleave: rows [256j, 256j+128) of W1 block j, [256j+128, 256j+256) of W3 block j
         ref13 = np.stack([dw1.reshape(I // 128, 128, cfg.d), dw3.reshape(I // 128, 128, cfg.d)], 1).reshape(2 * I, cfg.d)
-        errs[f"dw13[{e}]"] = rel_err(got["dw13"][e], ref13)
-        errs[f"dw2[{e}]"] = rel_err(got["dw2"][e], dw2)
+        werr[f"dw13[{e}]"] = fro_err(got["dw13"][e], ref13)
+        werr[f"dw2[{e}]"] = fro_err(got["dw2"][e], dw2)
     for e in set(range(cfg.E)) - set(ref["dw_routed"]):
         assert not got["dw13"][e].any() and not got["dw2"][e].any()
     for s, (dw1, dw3, dw2) in enumerate(ref["dw_shared"]):
         ref13 = np.stack([dw1.reshape(I // 128, 128, cfg.d), dw3.reshape(I // 128, 128, cfg.d)], 1).reshape(2 * I, cfg.d)
-        errs[f"dws13[{s}]"] = rel_err(got["dws13"][s], ref13)
-        errs[f"dws2[{s}]"] = rel_err(got["dws2"][s], dw2)
-    worst = max(errs, key=errs.get)
-    print(f"{name}: du {errs['du']:.3e}, dcentroids {errs['dcentroids']:.3e}, worst {worst} {errs[worst]:.3e}")
-    assert all(v <= BWD_TOL for v in errs.values()), {k: v for k, v in errs.items() if v > BWD_TOL}
+        werr[f"dws13[{s}]"] = fro_err(got["dws13"][s], ref13)
+        werr[f"dws2[{s}]"] = fro_err(got["dws2"][s], dw2)
+    worst = max(werr, key=werr.get)
+    print(f"{name}: weight gradients, worst {worst} {werr[worst]:.3e} (relative Frobenius)")
+    assert all(v <= WG_TOL for v in werr.values()), {k: v for k, v in werr.items() if v > WG_TOL}
+    # the weight-gradient GEMM's arithmetic: dW2 = dy^T h on the bf16-rounded operands
+    x = oracle.bf16_to_f64(synth.bf16_bits(u))
+    G = oracle.bf16_to_f64(synth.bf16_bits(dout))
+    gate = gate.cpu().numpy().astype(np.float64)
+    for e in sorted(ref["dw_routed"])[:4]:
+        w1, w3, _ = (oracle.bf16_to_f64(w) for w in host.routed_bits(e))
+        rows, js = np.nonzero(idx == e)
+        a, b = _bf16(x[rows] @ w1.T), _bf16(x[rows] @ w3.T)
+        h = _bf16(a / (1.0 + np.exp(-a)) * b)
+        dy = _bf16(gate[rows, js][:, None] * G[rows])
+        assert fro_err(got["dw2"][e], dy.T @ h) <= REPLAY_TOL, e
 
 
 def test_transpose_expert_weights():
