@@ -530,6 +530,38 @@ def measure_decode(args, world, pk, layer=None):
                          for m, g, x in zip(step_ms, gbs, c)]}
 
 
+def measure_backward(layer, cfg, u, bias, pk, steps=5, warmup=3):
+    """The layer's backward pass (bf16) on the same batch: dL/dh' a seeded
+    Gaussian, all gradients (du, dcentroids, every expert's dW in fp32)."""
+    layer.prepare_backward()
+    g = torch.Generator(device="cuda").manual_seed(1)
+    dout = torch.randn((cfg.T, cfg.d), device="cuda", generator=g).to(torch.bfloat16)
+    for _ in range(warmup):
+        grads = layer.backward(u, bias, dout)
+    torch.cuda.synchronize()
+    if layer.backward_status() != 0:
+        raise RuntimeError(f"backward device status {layer.backward_status()}")
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(steps):
+        grads = layer.backward(u, bias, dout)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    del grads
+    T, d, E, k, Ns, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.n_shared, cfg.inter
+    # algorithmic work: the forward's expert GEMMs recomputed, two data-gradient
+    # and two weight-gradient products per expert; bf16 weights read twice
+    # (w and its transpose), fp32 weight gradients written
+    F = 3 * 2 * T * (k + Ns) * 3 * d * I + 2 * T * d * E
+    B = (E + Ns) * 3 * d * I * (2 + 2 + 4) + E * d * (2 + 4) + T * d * (2 + 2 + 4)
+    t_f, t_b = F / (pk["bf16"] * 1e12), B / (pk["hbm"] * 1e9)
+    return {"value": round(T / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 3),
+            "tflops": round(F / (ms * 1e-3) / 1e12, 1), "gbs": round(B / (ms * 1e-3) / 1e9, 1),
+            "roofline_frac": round(max(t_f, t_b) / (ms * 1e-3), 4), "bound": "tensor" if t_f >= t_b else "hbm",
+            "algorithmic_flops": int(F), "algorithmic_bytes": int(B)}
+
+
 def cpu_baseline_leg(cfg, u_host, n_sample):
     """The oracle beside the GPU: routing of the whole batch, and the routing +
     full layer output of a strided sample of n_sample tokens (tokens are
@@ -552,8 +584,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="v3", choices=["v3", "v3_fp8", "mid", "decode", "v3_slice", "v3_slice_fp8",
-                                                            "decode_slice", "v3_tokens", "v3_tokens_fp8"])
+    ap.add_argument("--workload", default="v3", choices=["v3", "v3_fp8", "v3_ue8m0", "v3_nodes", "mid", "decode",
+                                                            "v3_slice", "v3_slice_fp8", "decode_slice", "v3_tokens",
+                                                            "v3_tokens_fp8"])
     ap.add_argument("--no-variants", action="store_true", help="skip the mid, FP8 and decode measurements")
     ap.add_argument("--prec", default=None, choices=["bf16", "fp8", "fp8_ue8m0"],
                     help="override the workload's precision")
@@ -614,6 +647,7 @@ def main():
 
     variants = {}
     if not args.no_variants and args.workload == "v3":
+        variants["v3_backward"] = measure_backward(layer, cfg, res["u_host"].cuda(), res["bias"], pk)
         del layer, res["layer"]
         torch.cuda.empty_cache()
         rm = measure(synth.get_config("mid"), args, world, pk)
@@ -627,6 +661,10 @@ def main():
         dec = measure_decode(args, world, pk, dec_layer.with_tokens(synth.get_config("decode").T))
         variants["decode_fp8"] = {k: v for k, v in dec.items() if k != "per_step"}
         del dec_layer
+        torch.cuda.empty_cache()
+        ru = measure(synth.get_config("v3_ue8m0"), args, world, pk)
+        variants["v3_fp8_ue8m0"] = variant_summary(ru)
+        del ru
         torch.cuda.empty_cache()
 
     cpu = None
