@@ -216,7 +216,8 @@ def stage_work(cfg, counts: np.ndarray):
         "router_gemm": (2 * T * d * E, T * d * 2 + E * d * 2 + T * E * 4),
         "topk": (0, T * E * 4 + R * 8),
         "scan_plan": (0, 0),
-        "gather": (0, T * d * 2 + R * d * xb + xs),
+        # FP8 with shared experts: the gather also writes u's own codes and scales once per token
+        "gather": (0, T * d * 2 + R * d * xb + xs + (T * d + T * (d // 128) * 4 if fp8 and Ns else 0)),
         "routed_gate_up": (2 * R * d * 2 * I, active * (2 * I * d * wb + s13) + R * d * xb + xs + R * I * xb + hs),
         "routed_down": (2 * R * I * d, active * (d * I * wb + s2) + R * I * xb + hs + R * d * 2),
         "shared_gate_up": (2 * Ns * T * d * 2 * I,
