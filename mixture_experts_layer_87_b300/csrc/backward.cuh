@@ -23,10 +23,11 @@ namespace moe {
 // Columns of the transposed activations for the weight-gradient GEMM: the rows
 // of group g (offsets[g] .. offsets[g+1]) become columns pad_off[g] .., every
 // group padded to a multiple of 64 columns (one 64-wide K stage of the GEMM;
-// the padding is zero).  One block: the prefix is serial (G is at most a few
-// thousand), the row -> column map is grid-strided by the same block.
-__global__ void __launch_bounds__(1024) pad_plan_kernel(const int32_t* __restrict__ offsets, int G, int rows,
-                                                        int32_t* __restrict__ pad_off, int32_t* __restrict__ col_of_row,
+// the padding is zero).  row_of_col[col] = the row a column holds, or -1 for
+// a padding column, for all n_cols columns.  One block: the prefix is serial
+// (G is at most a few thousand), the columns are block-strided.
+__global__ void __launch_bounds__(1024) pad_plan_kernel(const int32_t* __restrict__ offsets, int G, int n_cols,
+                                                        int32_t* __restrict__ pad_off, int32_t* __restrict__ row_of_col,
                                                         int* status) {
   __shared__ int s_off[2049];
   if (threadIdx.x == 0) {
@@ -36,48 +37,67 @@ __global__ void __launch_bounds__(1024) pad_plan_kernel(const int32_t* __restric
       pad_off[g] = acc;
       if (g < G) acc += (offsets[g + 1] - offsets[g] + 63) / 64 * 64;
     }
+    if (acc > n_cols) record_status(status, ST_BAD_INDEX);
   }
   __syncthreads();
   if (G > 2048) {  // not used by the library (G <= E + n_shared <= 2048)
     if (threadIdx.x == 0) record_status(status, ST_BAD_INDEX);
     return;
   }
-  for (int r = threadIdx.x; r < rows; r += blockDim.x) {
-    int lo = 0, hi = G;  // find g with offsets[g] <= r < offsets[g + 1]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (offsets[mid] <= r) lo = mid;
-      else hi = mid;
+  for (int col = threadIdx.x; col < n_cols; col += blockDim.x) {
+    int r = -1;
+    if (col < s_off[G]) {
+      int lo = 0, hi = G;  // g with s_off[g] <= col < s_off[g + 1]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_off[mid] <= col) lo = mid;
+        else hi = mid;
+      }
+      const int local = col - s_off[lo];
+      if (local < offsets[lo + 1] - offsets[lo]) r = offsets[lo] + local;
     }
-    col_of_row[r] = s_off[lo] + (r - offsets[lo]);
+    row_of_col[col] = r;
   }
 }
 
-// dst[c][col_of_row[r]] = src[r][c] for r < rows, c < C (bf16), batched over
-// blockIdx.z (src/dst strides per batch).  col_of_row == nullptr: the
-// identity.  32 x 32 tiles through shared memory, both sides coalesced.
+// Transposed gather, batched over blockIdx.z (src/dst strides per batch):
+//   dst[c][col] = src[row(col)][c]  for c < C, col < n_cols,
+// row(col) = row_of_col[col] (-1: a zero column) or, with row_of_col ==
+// nullptr, col itself while col < rows (zero beyond).  Every dst column is
+// written, padding included.  64 x 64 tiles through shared memory: 16-byte
+// loads along the src rows, 128 contiguous bytes per warp along the dst rows.
+// Needs C % 8 == 0, 16-byte aligned src rows and an even ldd.
 __global__ void __launch_bounds__(256) transpose_bf16_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C,
-                                                             int64_t src_batch, const int32_t* __restrict__ col_of_row,
-                                                             __nv_bfloat16* __restrict__ dst, int64_t ldd,
+                                                             int64_t src_batch, const int32_t* __restrict__ row_of_col,
+                                                             int n_cols, __nv_bfloat16* __restrict__ dst, int64_t ldd,
                                                              int64_t dst_batch) {
-  __shared__ __nv_bfloat16 tile[32][33];
+  __shared__ uint16_t tile[64][66];  // [c - c0][col - col0]
   src += blockIdx.z * src_batch;
   dst += blockIdx.z * dst_batch;
-  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  const int c0 = blockIdx.x * 64, col0 = blockIdx.y * 64, tid = threadIdx.x;
+  const int chunk = tid & 7;  // 8 columns c of the src row
 #pragma unroll
-  for (int i = 0; i < 32; i += 8) {
-    const int r = r0 + ty + i, c = c0 + tx;
-    if (r < rows && c < C) tile[ty + i][tx] = src[(int64_t)r * C + c];
+  for (int i = 0; i < 2; ++i) {
+    const int cl = (tid >> 3) + 32 * i, col = col0 + cl;
+    int r = -1;
+    if (col < n_cols) r = row_of_col ? row_of_col[col] : (col < rows ? col : -1);
+    const int c = c0 + chunk * 8;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r >= 0 && r < rows && c < C) v = *reinterpret_cast<const uint4*>(src + (int64_t)r * C + c);
+    const uint16_t* e = reinterpret_cast<const uint16_t*>(&v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) tile[chunk * 8 + j][cl] = e[j];
   }
   __syncthreads();
+  const int p = tid & 31;  // column pair col0 + 2p, + 1
 #pragma unroll
-  for (int i = 0; i < 32; i += 8) {
-    const int c = c0 + ty + i, r = r0 + tx;
-    if (r < rows && c < C) {
-      const int col = col_of_row ? col_of_row[r] : r;
-      dst[(int64_t)c * ldd + col] = tile[tx][ty + i];
-    }
+  for (int i = 0; i < 8; ++i) {
+    const int cl = (tid >> 5) + 8 * i, c = c0 + cl, col = col0 + 2 * p;
+    if (c >= C || col >= n_cols) continue;
+    const uint32_t pair = *reinterpret_cast<const uint32_t*>(&tile[cl][2 * p]);
+    __nv_bfloat16* o = dst + (int64_t)c * ldd + col;
+    if (col + 1 < n_cols) *reinterpret_cast<uint32_t*>(o) = pair;
+    else *reinterpret_cast<uint16_t*>(o) = static_cast<uint16_t>(pair & 0xFFFF);
   }
 }
 
@@ -85,35 +105,64 @@ __global__ void __launch_bounds__(256) transpose_bf16_kernel(const __nv_bfloat16
 // f / 128 sit at columns 256 (f / 128) + f % 128 (gate) and + 128 (up).
 __device__ __forceinline__ int64_t gate_col(int f) { return 256 * (f >> 7) + (f & 127); }
 
+// 8 bf16 <-> 8 floats
+__device__ __forceinline__ void unpack8_bf16(const uint4& v, float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 p = __bfloat1622float2(h[i]);
+    f[2 * i] = p.x;
+    f[2 * i + 1] = p.y;
+  }
+}
+__device__ __forceinline__ uint4 pack8_bf16(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+}
+
 // h = SiLU(a) * b from the stored pre-activations ab [rows, 2I] (bf16, w13
-// interleave) -> h [rows, I] bf16.
+// interleave) -> h [rows, I] bf16; 8 features per thread (I % 8 == 0, so
+// the 8 never straddle a 128-feature block).
 __global__ void swiglu_fwd_kernel(const __nv_bfloat16* __restrict__ ab, int64_t rows, int I,
                                   __nv_bfloat16* __restrict__ h) {
-  const int64_t n = rows * I;
+  const int I8 = I / 8;
+  const int64_t n = rows * I8;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / I;
-    const int f = static_cast<int>(i - r * I);
-    const __nv_bfloat16* row = ab + r * 2 * I;
-    const float a = __bfloat162float(row[gate_col(f)]), b = __bfloat162float(row[gate_col(f) + 128]);
-    h[i] = __float2bfloat16_rn(silu(a) * b);
+    const int64_t r = i / I8;
+    const int f = static_cast<int>(i - r * I8) * 8;
+    const __nv_bfloat16* row = ab + r * 2 * I + gate_col(f);
+    float a[8], b[8], o[8];
+    unpack8_bf16(*reinterpret_cast<const uint4*>(row), a);
+    unpack8_bf16(*reinterpret_cast<const uint4*>(row + 128), b);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) o[j] = silu(a[j]) * b[j];
+    *reinterpret_cast<uint4*>(h + r * I + f) = pack8_bf16(o);
   }
 }
 
 // SwiGLU backward: with sg = sigmoid(a), h = a sg b:
 //   da = dh b sg (1 + a (1 - sg)),  db = dh a sg
-// written into dab [rows, 2I] in the w13 interleave (the layout of ab).
+// written into dab [rows, 2I] in the w13 interleave (the layout of ab);
+// 8 features per thread.
 __global__ void swiglu_bwd_kernel(const __nv_bfloat16* __restrict__ ab, const __nv_bfloat16* __restrict__ dh,
                                   int64_t rows, int I, __nv_bfloat16* __restrict__ dab) {
-  const int64_t n = rows * I;
+  const int I8 = I / 8;
+  const int64_t n = rows * I8;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = i / I;
-    const int f = static_cast<int>(i - r * I);
+    const int64_t r = i / I8;
+    const int f = static_cast<int>(i - r * I8) * 8;
     const int64_t ca = r * 2 * I + gate_col(f);
-    const float a = __bfloat162float(ab[ca]), b = __bfloat162float(ab[ca + 128]);
-    const float g = __bfloat162float(dh[i]);
-    const float sg = 1.0f / (1.0f + __expf(-a));
-    dab[ca] = __float2bfloat16_rn(g * b * sg * (1.0f + a * (1.0f - sg)));
-    dab[ca + 128] = __float2bfloat16_rn(g * a * sg);
+    float a[8], b[8], g[8], da[8], db[8];
+    unpack8_bf16(*reinterpret_cast<const uint4*>(ab + ca), a);
+    unpack8_bf16(*reinterpret_cast<const uint4*>(ab + ca + 128), b);
+    unpack8_bf16(*reinterpret_cast<const uint4*>(dh + r * I + f), g);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float sg = 1.0f / (1.0f + __expf(-a[j]));
+      da[j] = g[j] * b[j] * sg * (1.0f + a[j] * (1.0f - sg));
+      db[j] = g[j] * a[j] * sg;
+    }
+    *reinterpret_cast<uint4*>(dab + ca) = pack8_bf16(da);
+    *reinterpret_cast<uint4*>(dab + ca + 128) = pack8_bf16(db);
   }
 }
 
@@ -150,16 +199,24 @@ __global__ void __launch_bounds__(128) combine_bwd_kernel(
     s_s[tid] = 1.0f / (1.0f + expf(-zz));
   }
   __syncthreads();
+  // 8 columns per thread per step (d % 8 == 0): 16-byte loads and stores
   const __nv_bfloat16* Gt = G + (int64_t)t * d;
+  const int d8 = d / 8;
   for (int j = 0; j < k; ++j) {
     const int sl = s_slot[j];
     float part = 0.0f;
     if (sl >= 0) {
       const float gj = s_g[j];
-      for (int c = tid; c < d; c += blockDim.x) {
-        const float gv = __bfloat162float(Gt[c]);
-        dy[(int64_t)sl * d + c] = __float2bfloat16_rn(gj * gv);
-        part = fmaf(gv, __bfloat162float(y[(int64_t)sl * d + c]), part);
+      for (int c8 = tid; c8 < d8; c8 += blockDim.x) {
+        float gv[8], yv[8], o[8];
+        unpack8_bf16(reinterpret_cast<const uint4*>(Gt)[c8], gv);
+        unpack8_bf16(reinterpret_cast<const uint4*>(y + (int64_t)sl * d)[c8], yv);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          o[i] = gj * gv[i];
+          part = fmaf(gv[i], yv[i], part);
+        }
+        reinterpret_cast<uint4*>(dy + (int64_t)sl * d)[c8] = pack8_bf16(o);
       }
     }
 #pragma unroll
@@ -188,28 +245,55 @@ __global__ void __launch_bounds__(128) combine_bwd_kernel(
     if (tid < k) s_dz[tid] = dz;
   }
   __syncthreads();
-  for (int c = tid; c < d; c += blockDim.x) {
-    float acc = __bfloat162float(Gt[c]);
-    for (int j = 0; j < k; ++j)
-      if (s_e[j] >= 0) acc = fmaf(s_dz[j], __bfloat162float(cent[(int64_t)s_e[j] * d + c]), acc);
-    du[(int64_t)t * d + c] = acc;
+  for (int c8 = tid; c8 < d8; c8 += blockDim.x) {
+    float acc[8];
+    unpack8_bf16(reinterpret_cast<const uint4*>(Gt)[c8], acc);
+    for (int j = 0; j < k; ++j) {
+      if (s_e[j] < 0) continue;
+      float cv[8];
+      unpack8_bf16(reinterpret_cast<const uint4*>(cent + (int64_t)s_e[j] * d)[c8], cv);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(s_dz[j], cv[i], acc[i]);
+    }
+    float4* o = reinterpret_cast<float4*>(du + (int64_t)t * d) + 2 * c8;
+    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
 }
 
-// du_t += sum_j dx[slot(t,j)] + sum_s dx_shared[s T + t]   (fp32 accumulation)
+// du_t += sum_j dx[slot(t,j)] + sum_s dx_shared[s T + t]   (fp32 accumulation,
+// 8 columns per thread: d % 8 == 0)
 __global__ void __launch_bounds__(128) gather_dx_kernel(const __nv_bfloat16* __restrict__ dx,
                                                         const int32_t* __restrict__ slot, int k, int64_t rows,
                                                         const __nv_bfloat16* __restrict__ dx_shared, int n_shared,
                                                         int T, int d, float* __restrict__ du) {
+  __shared__ int s_slot[32];
   const int t = blockIdx.x;
-  for (int c = threadIdx.x; c < d; c += blockDim.x) {
-    float acc = du[(int64_t)t * d + c];
+  if (threadIdx.x < k) {
+    const int s = slot[(int64_t)t * k + threadIdx.x];
+    s_slot[threadIdx.x] = s >= 0 && s < rows ? s : -1;
+  }
+  __syncthreads();
+  const int d8 = d / 8;
+  for (int c8 = threadIdx.x; c8 < d8; c8 += blockDim.x) {
+    float4* o = reinterpret_cast<float4*>(du + (int64_t)t * d) + 2 * c8;
+    const float4 lo = o[0], hi = o[1];
+    float acc[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
     for (int j = 0; j < k; ++j) {
-      const int s = slot[(int64_t)t * k + j];
-      if (s >= 0 && s < rows) acc += __bfloat162float(dx[(int64_t)s * d + c]);
+      if (s_slot[j] < 0) continue;
+      float v[8];
+      unpack8_bf16(reinterpret_cast<const uint4*>(dx + (int64_t)s_slot[j] * d)[c8], v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += v[i];
     }
-    for (int s = 0; s < n_shared; ++s) acc += __bfloat162float(dx_shared[((int64_t)s * T + t) * d + c]);
-    du[(int64_t)t * d + c] = acc;
+    for (int s = 0; s < n_shared; ++s) {
+      float v[8];
+      unpack8_bf16(reinterpret_cast<const uint4*>(dx_shared + ((int64_t)s * T + t) * d)[c8], v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += v[i];
+    }
+    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
 }
 

@@ -725,7 +725,7 @@ namespace {
 // followed by the backward's own buffers.
 struct BwdLayout {
   Layout f;
-  size_t queue, ab, dy, dh, dab, dx, dz_row, ab_s, dh_s, dab_s, dx_s, pad_off, col_of_row, wg_r, wg_s2, wg_s13;
+  size_t queue, ab, dy, dh, dab, dx, dz_row, ab_s, dh_s, dab_s, dx_s, pad_off, row_of_col, wg_r, wg_s2, wg_s13;
   size_t xT, dyT, hT, dabT, uT, GT, hsT, dabsT, total;
   int64_t Rp, Tp;
 };
@@ -754,7 +754,7 @@ BwdLayout make_bwd_layout(const moe_dims& d) {
   B.dab_s = take(Ns * T * 2 * I * 2);
   B.dx_s = take(Ns * T * D * 2);
   B.pad_off = take((E + 2) * 4);
-  B.col_of_row = take(R * 4);
+  B.row_of_col = take(B.Rp * 4);
   B.wg_r = take(E * sizeof(WgradGroup));
   B.wg_s2 = take((Ns + 1) * sizeof(WgradGroup));
   B.wg_s13 = take((Ns + 1) * sizeof(WgradGroup));
@@ -819,29 +819,57 @@ moe_status xgemm_bf16(const void* w, int64_t w_rows, int Nw, int K, const void* 
   return launch_xgemm<Epi::BF16>(tw, tx, a, chunks * cdiv(Nw, 256), st);
 }
 
-// Transposed copy src [batch][rows][C] -> dst: dst + b * dst_batch + c * ldd + col(r).
-moe_status transpose_bf16(const void* src, int rows, int C, int64_t src_batch, const int32_t* col_of_row, void* dst,
-                          int64_t ldd, int64_t dst_batch, int batch, cudaStream_t st) {
-  if (rows <= 0 || C <= 0 || batch <= 0) return MOE_OK;
-  dim3 grid(static_cast<unsigned>(cdiv(C, 32)), static_cast<unsigned>(cdiv(rows, 32)), static_cast<unsigned>(batch));
-  transpose_bf16_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, C, src_batch, col_of_row,
-                                               static_cast<__nv_bfloat16*>(dst), ldd, dst_batch);
+// Transposed gather src [batch][rows][C] -> dst [batch][C][n_cols] (row ldd):
+// dst column col holds src row row_of_col[col] (-1: zeros), or row col while
+// col < rows when row_of_col is null.
+moe_status transpose_bf16(const void* src, int rows, int C, int64_t src_batch, const int32_t* row_of_col,
+                          int64_t n_cols, void* dst, int64_t ldd, int64_t dst_batch, int batch, cudaStream_t st) {
+  if (n_cols <= 0 || C <= 0 || batch <= 0) return MOE_OK;
+  if (C % 8 || ldd % 2 || n_cols > INT_MAX) return MOE_ERR_UNSUPPORTED;
+  dim3 grid(static_cast<unsigned>(cdiv(C, 64)), static_cast<unsigned>(cdiv(n_cols, 64)), static_cast<unsigned>(batch));
+  transpose_bf16_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, C, src_batch, row_of_col,
+                                               static_cast<int>(n_cols), static_cast<__nv_bfloat16*>(dst), ldd,
+                                               dst_batch);
   return launched();
 }
 
 // Weight gradients of n_groups groups: out[g] [M, N] fp32 = A[:, ka..] . B[:, kb..]^T.
+// fp32 output [G][M][N] for TMA stores: boxes of 32 x 32 elements, 128-byte
+// swizzle (the layout the wgrad epilogue writes its staging boxes in).
+moe_status make_tmap_out3d(CUtensorMap* map, float* base, int64_t G, int64_t M, int64_t N) {
+  auto fn = encode_fn();
+  if (!fn) return MOE_ERR_CUDA;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(G)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(N * 4), static_cast<cuuint64_t>(M * N * 4)};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Weight gradients out[g] = A[:, ka_g ..] . B[:, kb_g ..]^T for n_groups groups
+// (persistent wgrad_gemm_kernel; queue: one zeroed item counter).
 moe_status wgrad(const void* A, int64_t a_cols, int M, const void* Bm, int64_t b_cols, int N,
-                 const WgradGroup* table, int n_groups, float* out, int* status, cudaStream_t st) {
+                 const WgradGroup* table, int n_groups, float* out, int* queue, int* status, cudaStream_t st) {
   if (n_groups <= 0) return MOE_OK;
-  CUtensorMap ta, tb;
+  if (N % 4) return MOE_ERR_UNSUPPORTED;  // fp32 rows of the output map: 16-byte multiples
+  CUtensorMap ta, tb, to;
   MOE_TRY(make_tmap(&ta, A, false, M, a_cols, 128));
   MOE_TRY(make_tmap(&tb, Bm, false, N, b_cols, 256));
-  WgradArgs a{table, M, N, out, status};
+  MOE_TRY(make_tmap_out3d(&to, out, n_groups, M, N));
+  WgradArgs a{table, n_groups, M, N, static_cast<int32_t>(cdiv(M, 128)), static_cast<int32_t>(cdiv(N, 256)), queue,
+              status};
+  const int64_t items = int64_t(n_groups) * a.m_tiles * a.n_tiles;
+  if (items > INT_MAX) return MOE_ERR_UNSUPPORTED;
+  int sms = 0;
+  MOE_TRY(sm_count(&sms));
+  const int64_t grid = items < sms ? items : sms;
   constexpr size_t smem = wgrad_smem_bytes();
   MOE_TRY(cuda_ok(cudaFuncSetAttribute(wgrad_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem))));
-  dim3 grid(static_cast<unsigned>(cdiv(N, 256)), static_cast<unsigned>(M / 128), static_cast<unsigned>(n_groups));
-  wgrad_gemm_kernel<<<grid, 192, smem, st>>>(ta, tb, a);
+  wgrad_gemm_kernel<<<static_cast<unsigned>(grid), kWgThreads, smem, st>>>(ta, tb, to, a);
   return launched();
 }
 
@@ -911,8 +939,8 @@ moe_status moe_transpose_expert_weights(int32_t n_experts, int32_t inter, int32_
   if (!w13 || !w2 || !w13t || !w2t) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t I2 = 2 * int64_t(inter);
-  MOE_TRY(transpose_bf16(w13, static_cast<int>(I2), d, I2 * d, nullptr, w13t, I2, I2 * d, n_experts, st));
-  return transpose_bf16(w2, d, inter, int64_t(d) * inter, nullptr, w2t, d, int64_t(d) * inter, n_experts, st);
+  MOE_TRY(transpose_bf16(w13, static_cast<int>(I2), d, I2 * d, nullptr, I2, w13t, I2, I2 * d, n_experts, st));
+  return transpose_bf16(w2, d, inter, int64_t(d) * inter, nullptr, d, w2t, d, int64_t(d) * inter, n_experts, st);
 }
 
 moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_weights_t* wt, const uint16_t* u,
@@ -924,6 +952,10 @@ moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_we
   const moe_dims& d = *dims;
   if (!wt || !wt->w13t || !wt->w2t || (d.n_shared > 0 && (!wt->ws13t || !wt->ws2t))) return MOE_ERR_INVALID_ARG;
   if (!gr || !gr->du || !gr->dcentroids || !gr->dw13 || !gr->dw2 || (d.n_shared > 0 && (!gr->dws13 || !gr->dws2)))
+    return MOE_ERR_INVALID_ARG;
+  // vector stores of du, TMA stores of the weight gradients
+  if (!aligned16(gr->du) || !aligned16(gr->dw13) || !aligned16(gr->dw2) ||
+      (d.n_shared > 0 && (!aligned16(gr->dws13) || !aligned16(gr->dws2))))
     return MOE_ERR_INVALID_ARG;
   if (!bias || (d.T > 0 && (!u || !dout)) || !aligned16(u) || !aligned16(dout)) return MOE_ERR_INVALID_ARG;
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1))) return MOE_ERR_INVALID_ARG;
@@ -970,7 +1002,7 @@ moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_we
   // --- routed experts: a, b (gate/up pre-activations), h, y
   MOE_TRY(xgemm_bf16(w->w13, E * I2, static_cast<int>(I2), static_cast<int>(D), x, R, ab, I2, static_cast<int>(E),
                      groups, mt_total, cgroup, chunks, 0, 0, queue + 0, status, st));
-  swiglu_fwd_kernel<<<ew_blocks(R * I), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab), R, static_cast<int>(I),
+  swiglu_fwd_kernel<<<ew_blocks(R * I / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab), R, static_cast<int>(I),
                                                        static_cast<__nv_bfloat16*>(h));
   MOE_TRY(launched());
   MOE_TRY(xgemm_bf16(w->w2, E * D, static_cast<int>(D), static_cast<int>(I), h, R, y, D, static_cast<int>(E), groups,
@@ -990,7 +1022,7 @@ moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_we
   void* dx = at<void>(ws, B.dx);
   MOE_TRY(xgemm_bf16(wt->w2t, E * I, static_cast<int>(I), static_cast<int>(D), dy, R, dh, I, static_cast<int>(E), groups,
                      mt_total, cgroup, chunks, 0, 0, queue + 2, status, st));
-  swiglu_bwd_kernel<<<ew_blocks(R * I), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab),
+  swiglu_bwd_kernel<<<ew_blocks(R * I / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab),
                                                        static_cast<const __nv_bfloat16*>(dh), R, static_cast<int>(I),
                                                        static_cast<__nv_bfloat16*>(dab));
   MOE_TRY(launched());
@@ -1006,12 +1038,12 @@ moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_we
     const int Ti = static_cast<int>(T), Nsi = static_cast<int>(Ns);
     MOE_TRY(xgemm_bf16(w->ws13, Ns * I2, static_cast<int>(I2), static_cast<int>(D), u, T, ab_s, I2, Nsi, nullptr,
                        nullptr, nullptr, 0, Ti, 0, queue + 4, status, st));
-    swiglu_fwd_kernel<<<ew_blocks(Ns * T * I), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab_s), Ns * T,
+    swiglu_fwd_kernel<<<ew_blocks(Ns * T * I / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab_s), Ns * T,
                                                               static_cast<int>(I), static_cast<__nv_bfloat16*>(h_s));
     MOE_TRY(launched());
     MOE_TRY(xgemm_bf16(wt->ws2t, Ns * I, static_cast<int>(I), static_cast<int>(D), dout, T, dh_s, I, Nsi, nullptr,
                        nullptr, nullptr, 0, Ti, 0, queue + 5, status, st));
-    swiglu_bwd_kernel<<<ew_blocks(Ns * T * I), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab_s),
+    swiglu_bwd_kernel<<<ew_blocks(Ns * T * I / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab_s),
                                                               static_cast<const __nv_bfloat16*>(dh_s), Ns * T,
                                                               static_cast<int>(I), static_cast<__nv_bfloat16*>(dab_s));
     MOE_TRY(launched());
@@ -1029,9 +1061,9 @@ moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_we
   MOE_TRY(launched());
   // --- weight gradients of the routed experts: the expert's tokens along K
   int32_t* pad_off = at<int32_t>(ws, B.pad_off);
-  int32_t* col_of_row = at<int32_t>(ws, B.col_of_row);
+  int32_t* row_of_col = at<int32_t>(ws, B.row_of_col);
   WgradGroup* wg_r = at<WgradGroup>(ws, B.wg_r);
-  pad_plan_kernel<<<1, 1024, 0, st>>>(offsets, static_cast<int>(E), static_cast<int>(R), pad_off, col_of_row, status);
+  pad_plan_kernel<<<1, 1024, 0, st>>>(offsets, static_cast<int>(E), static_cast<int>(B.Rp), pad_off, row_of_col, status);
   MOE_TRY(launched());
   wgrad_table_kernel<<<static_cast<unsigned>(cdiv(E, 256)), 256, 0, st>>>(pad_off, static_cast<int>(E), wg_r);
   MOE_TRY(launched());
@@ -1039,15 +1071,15 @@ moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_we
   void* dyT = at<void>(ws, B.dyT);
   void* hT = at<void>(ws, B.hT);
   void* dabT = at<void>(ws, B.dabT);
-  MOE_TRY(cuda_ok(cudaMemsetAsync(xT, 0, B.dabT + 2 * I2 * B.Rp - B.xT, st)));  // xT .. dabT: the zero padding
-  MOE_TRY(transpose_bf16(x, static_cast<int>(R), static_cast<int>(D), 0, col_of_row, xT, B.Rp, 0, 1, st));
-  MOE_TRY(transpose_bf16(dy, static_cast<int>(R), static_cast<int>(D), 0, col_of_row, dyT, B.Rp, 0, 1, st));
-  MOE_TRY(transpose_bf16(h, static_cast<int>(R), static_cast<int>(I), 0, col_of_row, hT, B.Rp, 0, 1, st));
-  MOE_TRY(transpose_bf16(dab, static_cast<int>(R), static_cast<int>(I2), 0, col_of_row, dabT, B.Rp, 0, 1, st));
+  // the padding columns are written as zeros by the transposes themselves
+  MOE_TRY(transpose_bf16(x, static_cast<int>(R), static_cast<int>(D), 0, row_of_col, B.Rp, xT, B.Rp, 0, 1, st));
+  MOE_TRY(transpose_bf16(dy, static_cast<int>(R), static_cast<int>(D), 0, row_of_col, B.Rp, dyT, B.Rp, 0, 1, st));
+  MOE_TRY(transpose_bf16(h, static_cast<int>(R), static_cast<int>(I), 0, row_of_col, B.Rp, hT, B.Rp, 0, 1, st));
+  MOE_TRY(transpose_bf16(dab, static_cast<int>(R), static_cast<int>(I2), 0, row_of_col, B.Rp, dabT, B.Rp, 0, 1, st));
   MOE_TRY(wgrad(dyT, B.Rp, static_cast<int>(D), hT, B.Rp, static_cast<int>(I), wg_r, static_cast<int>(E), gr->dw2,
-                status, st));
+                queue + 8, status, st));
   MOE_TRY(wgrad(dabT, B.Rp, static_cast<int>(I2), xT, B.Rp, static_cast<int>(D), wg_r, static_cast<int>(E), gr->dw13,
-                status, st));
+                queue + 9, status, st));
   // --- weight gradients of the shared experts (K = all tokens, padded)
   if (Ns > 0) {
     void* uT = at<void>(ws, B.uT);
@@ -1055,20 +1087,20 @@ moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_we
     void* hsT = at<void>(ws, B.hsT);
     void* dabsT = at<void>(ws, B.dabsT);
     const int Tp = static_cast<int>(B.Tp), Ti = static_cast<int>(T), Nsi = static_cast<int>(Ns);
-    MOE_TRY(cuda_ok(cudaMemsetAsync(uT, 0, B.dabsT + 2 * I2 * Ns * B.Tp - B.uT, st)));
-    MOE_TRY(transpose_bf16(u, Ti, static_cast<int>(D), 0, nullptr, uT, Tp, 0, 1, st));
-    MOE_TRY(transpose_bf16(dout, Ti, static_cast<int>(D), 0, nullptr, GT, Tp, 0, 1, st));
-    MOE_TRY(transpose_bf16(h_s, Ti, static_cast<int>(I), T * I, nullptr, hsT, Ns * Tp, Tp, Nsi, st));
-    MOE_TRY(transpose_bf16(dab_s, Ti, static_cast<int>(I2), T * I2, nullptr, dabsT, Ns * Tp, Tp, Nsi, st));
+    MOE_TRY(transpose_bf16(u, Ti, static_cast<int>(D), 0, nullptr, Tp, uT, Tp, 0, 1, st));
+    MOE_TRY(transpose_bf16(dout, Ti, static_cast<int>(D), 0, nullptr, Tp, GT, Tp, 0, 1, st));
+    MOE_TRY(transpose_bf16(h_s, Ti, static_cast<int>(I), T * I, nullptr, Tp, hsT, Ns * Tp, Tp, Nsi, st));
+    MOE_TRY(transpose_bf16(dab_s, Ti, static_cast<int>(I2), T * I2, nullptr, Tp, dabsT, Ns * Tp, Tp, Nsi, st));
     WgradGroup* wg_s2 = at<WgradGroup>(ws, B.wg_s2);
     WgradGroup* wg_s13 = at<WgradGroup>(ws, B.wg_s13);
     wgrad_strided_table_kernel<<<1, 256, 0, st>>>(Nsi, 0, Tp, Tp, wg_s2);       // A = G^T, B = h_s^T
     MOE_TRY(launched());
     wgrad_strided_table_kernel<<<1, 256, 0, st>>>(Nsi, Tp, 0, Tp, wg_s13);      // A = dab_s^T, B = u^T
     MOE_TRY(launched());
-    MOE_TRY(wgrad(GT, Tp, static_cast<int>(D), hsT, Ns * Tp, static_cast<int>(I), wg_s2, Nsi, gr->dws2, status, st));
-    MOE_TRY(wgrad(dabsT, Ns * Tp, static_cast<int>(I2), uT, Tp, static_cast<int>(D), wg_s13, Nsi, gr->dws13, status,
-                  st));
+    MOE_TRY(wgrad(GT, Tp, static_cast<int>(D), hsT, Ns * Tp, static_cast<int>(I), wg_s2, Nsi, gr->dws2, queue + 10,
+                  status, st));
+    MOE_TRY(wgrad(dabsT, Ns * Tp, static_cast<int>(I2), uT, Tp, static_cast<int>(D), wg_s13, Nsi, gr->dws13, queue + 11,
+                  status, st));
   }
   return MOE_OK;
 }
