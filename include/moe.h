@@ -308,6 +308,7 @@ moe_status moe_forward_replicated(const moe_dims* dims, const moe_weights* w, co
  *   w13t [n, d, 2I] = w13 [n, 2I, d] transposed per expert (the w13 row
  *   interleave becomes the column order), w2t [n, I, d] = w2 [n, d, I]
  *   transposed.  n = E for the routed experts, n_shared for the shared ones.
+ *   inter and d must be multiples of 128 (else MOE_ERR_INVALID_ARG).
  *
  * moe_backward recomputes the forward's routing, dispatch and expert
  * activations (the same kernels), then:
@@ -320,7 +321,8 @@ moe_status moe_forward_replicated(const moe_dims* dims, const moe_weights* w, co
  *   grads  outputs, all fp32 device memory: du [T, d]; dcentroids [E, d];
  *          dw13 [E, 2I, d] and dw2 [E, d, I] in the layout of w13 and w2 (an
  *          expert no token chose gets zeros); dws13, dws2 the same for the
- *          shared experts (unused when n_shared == 0).
+ *          shared experts (unused when n_shared == 0).  du and the weight
+ *          gradients must be 16-byte aligned (else MOE_ERR_INVALID_ARG).
  *   ws     at least moe_backward_workspace_size bytes.
  */
 typedef struct {
