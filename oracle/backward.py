@@ -18,12 +18,31 @@ given dL/dh' = G.  Readings where the pages are silent:
   * weight gradients are kept in high precision (section 3.3, item 1: master
     weights and weight gradients are stored in higher precision).
 Matrix products are numpy fp64 matmuls, expert by expert.
+
+fp8=True / "ue8m0": the fine-grained FP8 scheme of section 3.3 on all three
+GEMMs of every expert linear layer -- the forward product, the data gradient
+and the weight gradient (item 1) -- with E4M3 for every operand (item 4),
+weights in 128 x 128 blocks and activations and gradients in 1 x 128 tiles
+(item 2).  The pages do not say along which axis a gradient GEMM's tiles
+run; here, as in the forward, an activation or gradient operand is
+quantised along that GEMM's contraction axis (so one scale covers each
+promoted 128-long K block, item 3):
+  forward   x = Q_row(u) (along d), h' = Q_row(h) (along I), weights Q_blk(W);
+  dgrad     dh = Q_row(dy) Q_blk(W2), dx = Q_row(da) Q_blk(W1) + Q_row(db) Q_blk(W3);
+  wgrad     dW2 = Q_tok(dy)^T Q_tok(h), dW1 = Q_tok(da)^T Q_tok(u), dW3 = Q_tok(db)^T Q_tok(u),
+where Q_tok quantises each column in blocks of 128 consecutive tokens of the
+expert (token-ascending, the first block starting at the expert's first
+token; a short last block is padded with zeros) and the wgrad operands are
+the unquantised activations.  The quantisation is straight-through: the
+gradient of Q(x) is taken as that of x.  The router (affinities, gates,
+centroid gradient) stays in high precision (item 1).  Products of the
+dequantised operands are exact (fp64).
 """
 from __future__ import annotations
 
 import numpy as np
 
-from . import bf16_to_f64
+from . import bf16_to_f64, fp8_roundtrip_1x128, fp8_roundtrip_128x128
 
 
 def _sigmoid(a):
@@ -47,37 +66,76 @@ def swiglu_backward(x, w1, w3, w2, dy):
     return dx, da.T @ x, db.T @ x, dy.T @ h, y
 
 
-def layer_backward(u_bits, cent_bits, idx, G, routed_weights, shared_weights, n_shared: int, E: int) -> dict:
+def _q_tok(m: np.ndarray, pow2: bool) -> np.ndarray:
+    """Q_tok: 1 x 128 tiles along the token axis (axis 0) of m [n, C], blocks of
+    128 consecutive rows from row 0, a short last block padded with zeros."""
+    n, C = m.shape
+    n_pad = -(-n // 128) * 128
+    t = np.zeros((C, n_pad))
+    t[:, :n] = m.T
+    return fp8_roundtrip_1x128(t, pow2)[:, :n].T
+
+
+def _expert_backward_fp8(x, w1, w3, w2, dy, pow2):
+    """swiglu_backward in the FP8 scheme (module docstring): x [n, d] the
+    unquantised input rows, w* the unquantised weights, dy [n, d]."""
+    q_row = lambda m: fp8_roundtrip_1x128(m, pow2)
+    w1q, w3q, w2q = (fp8_roundtrip_128x128(w, pow2) for w in (w1, w3, w2))
+    xq = q_row(x)
+    a = xq @ w1q.T
+    b = xq @ w3q.T
+    sg = _sigmoid(a)
+    h = a * sg * b
+    y = q_row(h) @ w2q.T
+    dh = q_row(dy) @ w2q
+    da = dh * b * sg * (1.0 + a * (1.0 - sg))
+    db = dh * a * sg
+    dx = q_row(da) @ w1q + q_row(db) @ w3q
+    ut = _q_tok(x, pow2)
+    dyt, ht, dat, dbt = (_q_tok(m, pow2) for m in (dy, h, da, db))
+    return dx, dat.T @ ut, dbt.T @ ut, dyt.T @ ht, y
+
+
+def layer_backward(u_bits, cent_bits, idx, G, routed_weights, shared_weights, n_shared: int, E: int,
+                   fp8=False) -> dict:
     """Gradients of the layer for dL/dh' = G [T, d], the selection idx [T, k]
     held fixed.  routed_weights(e) / shared_weights(s) return bf16 bit patterns
     (W1, W3, W2).  Returns dict(du [T, d], dcent [E, d], dw_routed {e: (dW1,
     dW3, dW2)} for every selected expert, dw_shared [(dW1, dW3, dW2)] per
-    shared expert, gate [T, k], dgate [T, k])."""
+    shared expert, gate [T, k], dgate [T, k]).  fp8: False, True (amax/448
+    scales) or "ue8m0" (power-of-two scales): the FP8 scheme of the module
+    docstring, whose forward is that of oracle.layer_output(fp8=...)."""
     x = bf16_to_f64(u_bits)
     cent = bf16_to_f64(cent_bits)
     G = np.asarray(G, np.float64)
     T, d = x.shape
     k = idx.shape[1]
     idx = np.asarray(idx, np.int64)
+    pow2 = fp8 == "ue8m0"
+
+    def expert(xr, ws, dy):
+        w1, w3, w2 = (bf16_to_f64(w) for w in ws)
+        if fp8:
+            return _expert_backward_fp8(xr, w1, w3, w2, dy, pow2)
+        return swiglu_backward(xr, w1, w3, w2, dy)
+
     s_sel = _sigmoid(np.einsum("td,tjd->tj", x, cent[idx]))
     S = s_sel.sum(1, keepdims=True)
     gate = s_sel / S
     du = G.copy()                                    # the residual
     dw_shared = []
     for s in range(n_shared):
-        w1, w3, w2 = (bf16_to_f64(w) for w in shared_weights(s))
-        dx, dw1, dw3, dw2, _ = swiglu_backward(x, w1, w3, w2, G)
+        dx, dw1, dw3, dw2, _ = expert(x, shared_weights(s), G)
         du += dx
         dw_shared.append((dw1, dw3, dw2))
     dgate = np.zeros((T, k))
     dw_routed = {}
     for e in range(E):
-        rows, js = np.nonzero(idx == e)
+        rows, js = np.nonzero(idx == e)               # token-ascending
         if rows.size == 0:
             continue
-        w1, w3, w2 = (bf16_to_f64(w) for w in routed_weights(e))
         dy = gate[rows, js][:, None] * G[rows]
-        dx, dw1, dw3, dw2, y = swiglu_backward(x[rows], w1, w3, w2, dy)
+        dx, dw1, dw3, dw2, y = expert(x[rows], routed_weights(e), dy)
         np.add.at(du, rows, dx)
         dgate[rows, js] = (G[rows] * y).sum(1)
         dw_routed[e] = (dw1, dw3, dw2)

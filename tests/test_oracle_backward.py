@@ -119,3 +119,141 @@ def test_backward_matches_central_differences():
         fd = (loss(*plus(v)) - loss(*minus(v))) / (2 * eps)
         an = float((grad * v).sum())
         assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (what, fd, an)
+
+
+# ----------------------------------------------------------------------------
+# The FP8 backward (ai.flicky.cc 3.3: forward, data-gradient and weight-gradient
+# GEMMs in FP8, E4M3 everywhere, 1 x 128 activation tiles and 128 x 128 weight
+# blocks, tiles along each GEMM's contraction axis).  The independent
+# statement: torch autograd over the same layer, with every expert linear
+# layer an autograd Function that quantises its operands (brute.quant_dequant,
+# which shares no code with the oracle's C quantiser) and the rest (SwiGLU,
+# gates, router, residual) differentiated by autograd itself.
+from oracle import brute  # noqa: E402
+
+
+def _q_row(m, pow2):
+    return brute.quant_dequant(m, 1, 128, pow2)
+
+
+def _q_tok(m, pow2):
+    n, C = m.shape
+    n_pad = -(-n // 128) * 128
+    pad = np.zeros((n_pad, C))
+    pad[:n] = m
+    return brute.quant_dequant(pad, 128, 1, pow2)[:n]
+
+
+def _fp8_linear(pow2):
+    class Fp8Linear(torch.autograd.Function):
+        """y = Q_row(x) Q_blk(W)^T; dx = Q_row(dy) Q_blk(W); dW = Q_tok(dy)^T Q_tok(x)."""
+
+        @staticmethod
+        def forward(ctx, x, w):
+            ctx.save_for_backward(x, w)
+            xn, wn = x.detach().numpy(), w.detach().numpy()
+            return torch.from_numpy(_q_row(xn, pow2) @ brute.quant_dequant(wn, 128, 128, pow2).T)
+
+        @staticmethod
+        def backward(ctx, gy):
+            x, w = ctx.saved_tensors
+            xn, wn, gn = x.numpy(), w.numpy(), gy.numpy()
+            dx = _q_row(gn, pow2) @ brute.quant_dequant(wn, 128, 128, pow2)
+            dw = _q_tok(gn, pow2).T @ _q_tok(xn, pow2)
+            return torch.from_numpy(dx), torch.from_numpy(dw)
+
+    return Fp8Linear.apply
+
+
+def _dense_fp8_grads(cfg, u, c, routed, shared, idx, G, pow2):
+    lin = _fp8_linear(pow2)
+    ut = u.double().requires_grad_()
+    ct = c.double().requires_grad_()
+    rt = [tuple(w.double().requires_grad_() for w in ws) for ws in routed]
+    st = [tuple(w.double().requires_grad_() for w in ws) for ws in shared]
+
+    def ffn(x, ws):
+        w1, w3, w2 = ws
+        return lin(F.silu(lin(x, w1)) * lin(x, w3), w2)
+
+    mask = torch.zeros((cfg.T, cfg.E), dtype=torch.float64)
+    mask[torch.arange(cfg.T)[:, None], torch.from_numpy(idx.astype(np.int64))] = 1.0
+    s = torch.sigmoid(ut @ ct.T) * mask
+    g = s / s.sum(1, keepdim=True)
+    out = ut
+    for ws in st:
+        out = out + ffn(ut, ws)
+    for e in range(cfg.E):
+        rows = torch.from_numpy(np.nonzero((idx == e).any(1))[0])   # token-ascending
+        if rows.numel() == 0:
+            continue
+        out = out.index_add(0, rows, g[rows, e:e + 1] * ffn(ut[rows], rt[e]))
+    (out * torch.from_numpy(G)).sum().backward()
+    return ut.grad.numpy(), ct.grad.numpy(), [[w.grad for w in ws] for ws in rt], [[w.grad.numpy() for w in ws]
+                                                                                       for ws in st]
+
+
+def _fp8_setup(name, fp8):
+    cfg = synth.get_config(name)
+    u, c = synth.tokens(cfg), synth.centroids(cfg)
+    b = np.asarray(synth.normal_f32(4245, (cfg.E,), 0.02))
+    routed = [synth.expert_weights(cfg, e) for e in range(cfg.E)]
+    shared = [synth.expert_weights(cfg, s, shared=True) for s in range(cfg.n_shared)]
+    idx = oracle.route(synth.bf16_bits(u), synth.bf16_bits(c), b, cfg.k)["idx"]
+    G = np.random.default_rng(11).standard_normal((cfg.T, cfg.d))
+    bits = lambda ws: tuple(synth.bf16_bits(w) for w in ws)
+    run = lambda: ob.layer_backward(synth.bf16_bits(u), synth.bf16_bits(c), idx, G, lambda e: bits(routed[e]),
+                                    lambda s: bits(shared[s]), cfg.n_shared, cfg.E, fp8=fp8)
+    return cfg, u, c, routed, shared, idx, G, run
+
+
+def _max_rel(got, ref):
+    return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-300))
+
+
+def _compare_fp8(res, ref, cfg):
+    du, dc, dr, dsh = ref
+    errs = [_max_rel(res["du"], du), _max_rel(res["dcent"], dc)]
+    for e in range(cfg.E):
+        if e in res["dw_routed"]:
+            errs += [_max_rel(got, w.numpy()) for got, w in zip(res["dw_routed"][e], dr[e])]
+        else:
+            assert all(w is None or float(w.abs().max()) == 0 for w in dr[e])
+    for s in range(cfg.n_shared):
+        errs += [_max_rel(got, w) for got, w in zip(res["dw_shared"][s], dsh[s])]
+    return max(errs)
+
+
+@pytest.mark.parametrize("name,fp8", [("tiny", True), ("ragged", True), ("tiny", "ue8m0"), ("ragged", "ue8m0")])
+def test_fp8_backward_equals_autograd_with_fp8_linear_layers(name, fp8):
+    cfg, u, c, routed, shared, idx, G, run = _fp8_setup(name, fp8)
+    ref = _dense_fp8_grads(cfg, u, c, routed, shared, idx, G, fp8 == "ue8m0")
+    assert _compare_fp8(run(), ref, cfg) <= 1e-10
+
+
+def test_fp8_backward_differs_from_bf16_by_the_quantisation():
+    """The FP8 gradients are the bf16 ones up to E4M3's relative step (2^-4 per
+    operand, a few operands per product): close, but not equal."""
+    cfg, u, c, routed, shared, idx, G, run = _fp8_setup("ragged", True)
+    f = run()
+    ref = ob.layer_backward(synth.bf16_bits(u), synth.bf16_bits(c), idx, G,
+                            lambda e: tuple(synth.bf16_bits(w) for w in routed[e]),
+                            lambda s: tuple(synth.bf16_bits(w) for w in shared[s]), cfg.n_shared, cfg.E)
+    for key in ("du", "dcent"):
+        err = _max_rel(f[key], ref[key])
+        assert 1e-4 < err < 0.2, (key, err)
+
+
+@pytest.mark.parametrize("slip", ["wgrad_unquantised", "wgrad_tiles_along_features", "weights_unquantised"])
+def test_fp8_backward_statement_catches_planted_slips(monkeypatch, slip):
+    """Slips planted in the oracle's FP8 backward move it far from the autograd
+    statement, so the agreement above is not vacuous."""
+    cfg, u, c, routed, shared, idx, G, run = _fp8_setup("ragged", True)
+    ref = _dense_fp8_grads(cfg, u, c, routed, shared, idx, G, False)
+    if slip == "wgrad_unquantised":
+        monkeypatch.setattr(ob, "_q_tok", lambda m, pow2: m)
+    elif slip == "wgrad_tiles_along_features":
+        monkeypatch.setattr(ob, "_q_tok", lambda m, pow2: oracle.fp8_roundtrip_1x128(m, pow2))
+    else:
+        monkeypatch.setattr(ob, "fp8_roundtrip_128x128", lambda w, pow2=False: w)
+    assert _compare_fp8(run(), ref, cfg) > 1e-4
