@@ -532,8 +532,9 @@ def measure_decode(args, world, pk, layer=None):
 
 
 def measure_backward(layer, cfg, u, bias, pk, steps=5, warmup=3):
-    """The layer's backward pass (bf16) on the same batch: dL/dh' a seeded
-    Gaussian, all gradients (du, dcentroids, every expert's dW in fp32)."""
+    """The layer's backward pass on the same batch (bf16, or the FP8 scheme for
+    an FP8 layer): dL/dh' a seeded Gaussian, all gradients (du, dcentroids,
+    every expert's dW in fp32)."""
     layer.prepare_backward()
     g = torch.Generator(device="cuda").manual_seed(1)
     dout = torch.randn((cfg.T, cfg.d), device="cuda", generator=g).to(torch.bfloat16)
@@ -552,11 +553,19 @@ def measure_backward(layer, cfg, u, bias, pk, steps=5, warmup=3):
     del grads
     T, d, E, k, Ns, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.n_shared, cfg.inter
     # algorithmic work: the forward's expert GEMMs recomputed, two data-gradient
-    # and two weight-gradient products per expert; bf16 weights read twice
-    # (w and its transpose), fp32 weight gradients written
-    F = 3 * 2 * T * (k + Ns) * 3 * d * I + 2 * T * d * E
-    B = (E + Ns) * 3 * d * I * (2 + 2 + 4) + E * d * (2 + 4) + T * d * (2 + 2 + 4)
-    t_f, t_b = F / (pk["bf16"] * 1e12), B / (pk["hbm"] * 1e9)
+    # and two weight-gradient products per expert; weights read twice (w and
+    # its transpose; 1 byte each in FP8), fp32 weight gradients written.  In
+    # the FP8 scheme the recompute and the data gradients run on the FP8
+    # tensor path and the weight gradients on the bf16 one.
+    wb = 1 if cfg.is_fp8 else 2
+    f_ffn = 2 * T * (k + Ns) * 3 * d * I
+    F = 3 * f_ffn + 2 * T * d * E
+    B = (E + Ns) * 3 * d * I * (wb + wb + 4) + E * d * (2 + 4) + T * d * (2 + 2 + 4)
+    if cfg.is_fp8 and pk.get("fp8"):
+        t_f = 2 * f_ffn / (pk["fp8"] * 1e12) + (f_ffn + 2 * T * d * E) / (pk["bf16"] * 1e12)
+    else:
+        t_f = F / (pk["bf16"] * 1e12)
+    t_b = B / (pk["hbm"] * 1e9)
     return {"value": round(T / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 3),
             "tflops": round(F / (ms * 1e-3) / 1e12, 1), "gbs": round(B / (ms * 1e-3) / 1e9, 1),
             "roofline_frac": round(max(t_f, t_b) / (ms * 1e-3), 4), "bound": "tensor" if t_f >= t_b else "hbm",
@@ -657,8 +666,14 @@ def main():
         torch.cuda.empty_cache()
         r8 = measure(synth.get_config("v3_fp8"), args, world, pk)
         variants["v3_fp8"] = variant_summary(r8)
+        variants["v3_fp8_backward"] = measure_backward(r8["layer"], synth.get_config("v3_fp8"), r8["u_host"].cuda(),
+                                                       r8["bias"], pk)
         dec_layer = r8["layer"]
+        dec_layer.__dict__.pop("ws_bwd", None)   # the backward's workspace and transposed weights are not needed
+        for name in ("w13t", "w2t", "ws13t", "ws2t", "w13t_scale", "w2t_scale", "ws13t_scale", "ws2t_scale"):
+            dec_layer.__dict__.pop(name, None)
         del r8
+        torch.cuda.empty_cache()
         dec = measure_decode(args, world, pk, dec_layer.with_tokens(synth.get_config("decode").T))
         variants["decode_fp8"] = {k: v for k, v in dec.items() if k != "per_step"}
         del dec_layer

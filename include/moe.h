@@ -293,12 +293,12 @@ moe_status moe_forward_replicated(const moe_dims* dims, const moe_weights* w, co
                                   void* ws, size_t ws_bytes, void* stream);
 
 /*
- * Backward pass of the layer (bf16 layers only; MOE_ERR_UNSUPPORTED for FP8).
- * Given dL/dh' (dout), the gradients of the layer equation of ai.flicky.cc
- * 2.1.2 (xyznot.com Method 2) with respect to its input u, the router
- * centroids and every expert weight.  The selection is held fixed -- the
- * gradient flows through the gate values g = s / sum s, not through the top-k
- * choice -- and the bias, which the pages update by the sign rule
+ * Backward pass of the layer, bf16 or in the FP8 scheme (prec MOE_FP8_E4M3 or
+ * MOE_FP8_UE8M0).  Given dL/dh' (dout), the gradients of the layer equation of
+ * ai.flicky.cc 2.1.2 (xyznot.com Method 2) with respect to its input u, the
+ * router centroids and every expert weight.  The selection is held fixed --
+ * the gradient flows through the gate values g = s / sum s, not through the
+ * top-k choice -- and the bias, which the pages update by the sign rule
  * (moe_bias_update), gets no gradient.  Weight and centroid gradients are
  * fp32 (ai.flicky.cc 3.3 item 1: weight gradients are kept in higher
  * precision); activations inside are bf16, as in the forward.
@@ -309,6 +309,9 @@ moe_status moe_forward_replicated(const moe_dims* dims, const moe_weights* w, co
  *   interleave becomes the column order), w2t [n, I, d] = w2 [n, d, I]
  *   transposed.  n = E for the routed experts, n_shared for the shared ones.
  *   inter and d must be multiples of 128 (else MOE_ERR_INVALID_ARG).
+ *   FP8: moe_quantize_fp8_blocks of the transposed bf16 weights (a 128 x 128
+ *   block has the same scale either way round) gives the codes and the
+ *   w13t_scale [n, d/128, 2I/128] / w2t_scale [n, I/128, d/128] grids.
  *
  * moe_backward recomputes the forward's routing, dispatch and expert
  * activations (the same kernels), then:
@@ -317,6 +320,18 @@ moe_status moe_forward_replicated(const moe_dims* dims, const moe_weights* w, co
  *   dx = [da db] W13;  du = G + sum_j dx_j + sum_s dx_s + sum_j dz_j c_{e_j};
  *   dW2 = dy^T h, dW13 = [da db]^T x per expert (fp32 GEMMs over the expert's
  *   tokens), dcentroids_e = sum over its tokens of dz u.
+ * FP8 (ai.flicky.cc 3.3 items 1-4: forward, data-gradient and weight-gradient
+ * GEMMs in E4M3, weights in 128 x 128 blocks, activations and gradients in
+ * 1 x 128 tiles along each GEMM's contraction axis):
+ *   forward  as moe_forward in FP8 (a, b kept as bf16; h quantised along I);
+ *   dgrad    dh = Q(dy) Q(W2), dx = Q([da db]) Q(W13): the FP8 expert GEMM,
+ *            dy and [da db] quantised per 1 x 128 tile along their rows;
+ *   wgrad    dW2 = Q_t(dy)^T Q_t(h), dW13 = Q_t([da db])^T Q_t(u): every
+ *            operand quantised to E4M3 in 1 x 128 tiles along the tokens of
+ *            its expert (blocks from the expert's first token), then the
+ *            product of the dequantised values on the bf16 tensor cores with
+ *            fp32 accumulation (each dequantised value rounded to bf16: exact
+ *            for UE8M0 scales, within 2^-9 relative otherwise).
  *   dout   [T, d] bf16 dL/dh'.
  *   grads  outputs, all fp32 device memory: du [T, d]; dcentroids [E, d];
  *          dw13 [E, 2I, d] and dw2 [E, d, I] in the layout of w13 and w2 (an
@@ -326,10 +341,14 @@ moe_status moe_forward_replicated(const moe_dims* dims, const moe_weights* w, co
  *   ws     at least moe_backward_workspace_size bytes.
  */
 typedef struct {
-  const void* w13t;   /* [E, d, 2I] bf16 */
-  const void* w2t;    /* [E, I, d] bf16 */
-  const void* ws13t;  /* [n_shared, d, 2I] bf16 */
-  const void* ws2t;   /* [n_shared, I, d] bf16 */
+  const void* w13t;          /* [E, d, 2I] bf16, or E4M3 codes (FP8) */
+  const void* w2t;           /* [E, I, d] */
+  const void* ws13t;         /* [n_shared, d, 2I] */
+  const void* ws2t;          /* [n_shared, I, d] */
+  const float* w13t_scale;   /* FP8 only: [E, d/128, 2I/128] block scales; NULL for bf16 */
+  const float* w2t_scale;    /* FP8 only: [E, I/128, d/128] */
+  const float* ws13t_scale;  /* FP8 only: [n_shared, d/128, 2I/128] */
+  const float* ws2t_scale;   /* FP8 only: [n_shared, I/128, d/128] */
 } moe_weights_t;
 
 typedef struct {
@@ -344,6 +363,19 @@ typedef struct {
 moe_status moe_backward_workspace_size(const moe_dims* dims, size_t* bytes);
 moe_status moe_transpose_expert_weights(int32_t n_experts, int32_t inter, int32_t d, const uint16_t* w13,
                                         const uint16_t* w2, uint16_t* w13t, uint16_t* w2t, void* stream);
+/*
+ * FP8 weights transposed for the backward: the E4M3 codes of w13 [n, 2I, d] /
+ * w2 [n, d, I] and their block-scale grids [n, 2I/128, d/128] / [n, d/128,
+ * I/128] become w13t [n, d, 2I] / w2t [n, I, d] with w13t_scale [n, d/128,
+ * 2I/128] / w2t_scale [n, I/128, d/128].  A 128 x 128 block keeps its codes
+ * and its scale when transposed, so this equals moe_quantize_fp8_blocks of the
+ * transposed bf16 weights.  inter and d multiples of 128, 16-byte aligned
+ * codes (else MOE_ERR_INVALID_ARG).  Asynchronous on `stream`.
+ */
+moe_status moe_transpose_expert_weights_fp8(int32_t n_experts, int32_t inter, int32_t d, const uint8_t* w13,
+                                            const float* w13_scale, const uint8_t* w2, const float* w2_scale,
+                                            uint8_t* w13t, float* w13t_scale, uint8_t* w2t, float* w2t_scale,
+                                            void* stream);
 moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_weights_t* wt, const uint16_t* u,
                         const float* bias, const uint16_t* dout, const moe_grads* grads, void* ws, size_t ws_bytes,
                         void* stream);

@@ -25,6 +25,7 @@ EXPORTS = (
     "moe_status_string", "moe_workspace_size", "moe_route", "moe_route_noalloc", "moe_permute", "moe_grouped_ffn",
     "moe_combine", "moe_bias_update", "moe_forward", "moe_forward_profiled", "moe_forward_replicated",
     "moe_plan_replicas", "moe_backward", "moe_backward_workspace_size", "moe_transpose_expert_weights",
+    "moe_transpose_expert_weights_fp8",
     "moe_pack_gate_up",
     "moe_quantize_fp8_blocks",
     "moe_read_device_status", "moe_selftest_wait_timeout",
@@ -45,7 +46,8 @@ class moe_dims(ctypes.Structure):
 
 class moe_weights_t(ctypes.Structure):
     _fields_ = [("w13t", ctypes.c_void_p), ("w2t", ctypes.c_void_p), ("ws13t", ctypes.c_void_p),
-                ("ws2t", ctypes.c_void_p)]
+                ("ws2t", ctypes.c_void_p), ("w13t_scale", ctypes.c_void_p), ("w2t_scale", ctypes.c_void_p),
+                ("ws13t_scale", ctypes.c_void_p), ("ws2t_scale", ctypes.c_void_p)]
 
 
 class moe_grads(ctypes.Structure):
@@ -89,6 +91,7 @@ def lib() -> ctypes.CDLL:
             "moe_plan_replicas": ([i32, vp, i32, vp, vp, vp], ctypes.c_int),
             "moe_backward_workspace_size": ([D, ctypes.POINTER(sz)], ctypes.c_int),
             "moe_transpose_expert_weights": ([i32, i32, i32, vp, vp, vp, vp, vp], ctypes.c_int),
+            "moe_transpose_expert_weights_fp8": ([i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
             "moe_backward": ([D, ctypes.POINTER(moe_weights), ctypes.POINTER(moe_weights_t), vp, vp, vp,
                               ctypes.POINTER(moe_grads), vp, sz, vp], ctypes.c_int),
             "moe_pack_gate_up": ([vp, vp, i32, i32, i32, vp, vp], ctypes.c_int),
@@ -260,6 +263,13 @@ def moe_backward_workspace_size(dm: moe_dims) -> int:
 def moe_transpose_expert_weights(n_experts, inter, d, w13, w2, w13t, w2t, stream=None):
     _check(lib().moe_transpose_expert_weights(int(n_experts), int(inter), int(d), _ptr(w13), _ptr(w2), _ptr(w13t),
                                               _ptr(w2t), _stream(stream)), "moe_transpose_expert_weights")
+
+
+def moe_transpose_expert_weights_fp8(n_experts, inter, d, w13, w13_scale, w2, w2_scale, w13t, w13t_scale, w2t,
+                                     w2t_scale, stream=None):
+    _check(lib().moe_transpose_expert_weights_fp8(int(n_experts), int(inter), int(d), _ptr(w13), _ptr(w13_scale),
+                                                  _ptr(w2), _ptr(w2_scale), _ptr(w13t), _ptr(w13t_scale), _ptr(w2t),
+                                                  _ptr(w2t_scale), _stream(stream)), "moe_transpose_expert_weights_fp8")
 
 
 def moe_backward(dm, weights: moe_weights, weights_t: moe_weights_t, u, bias, dout, grads: moe_grads, ws, stream=None):

@@ -12,6 +12,8 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "gemm.cuh"
 #include "kernels.cuh"
@@ -22,20 +24,21 @@ namespace moe {
 // ---------------------------------------------------------------------------
 // Columns of the transposed activations for the weight-gradient GEMM: the rows
 // of group g (offsets[g] .. offsets[g+1]) become columns pad_off[g] .., every
-// group padded to a multiple of 64 columns (one 64-wide K stage of the GEMM;
-// the padding is zero).  row_of_col[col] = the row a column holds, or -1 for
+// group padded to a multiple of `gran` columns (64: one 64-wide K stage of the
+// GEMM; 128 in the FP8 scheme, so that 128-token quantisation blocks start at
+// every group's first token; the padding is zero).  row_of_col[col] = the row a column holds, or -1 for
 // a padding column, for all n_cols columns.  One block: the prefix is serial
 // (G is at most a few thousand), the columns are block-strided.
 __global__ void __launch_bounds__(1024) pad_plan_kernel(const int32_t* __restrict__ offsets, int G, int n_cols,
-                                                        int32_t* __restrict__ pad_off, int32_t* __restrict__ row_of_col,
-                                                        int* status) {
+                                                        int gran, int32_t* __restrict__ pad_off,
+                                                        int32_t* __restrict__ row_of_col, int* status) {
   __shared__ int s_off[2049];
   if (threadIdx.x == 0) {
     int acc = 0;
     for (int g = 0; g <= G; ++g) {
       if (g <= 2048) s_off[g] = acc;
       pad_off[g] = acc;
-      if (g < G) acc += (offsets[g + 1] - offsets[g] + 63) / 64 * 64;
+      if (g < G) acc += (offsets[g + 1] - offsets[g] + gran - 1) / gran * gran;
     }
     if (acc > n_cols) record_status(status, ST_BAD_INDEX);
   }
@@ -101,20 +104,170 @@ __global__ void __launch_bounds__(256) transpose_bf16_kernel(const __nv_bfloat16
   }
 }
 
+// Transposed gather with the FP8 quantisation of the weight-gradient operands
+// (1 x 128 tiles along the tokens, ai.flicky.cc 3.3 items 2 and 4), written
+// back dequantised as bf16 for the weight-gradient GEMM:
+//   dst[c][col] = bf16( E4M3(x * (1/s)) * s ),  x = src[row(col)][c],
+// s = amax/448 over the 128-column block of col (UE8M0: rounded up to a power
+// of two; an all-zero block: 1), 1/s one correctly rounded fp32 reciprocal
+// per block (the operands are intermediates known to bf16 accuracy; a
+// division per element would cost more than the copy).  row(col)
+// = perm[row_of_col[col]] when perm is given, else row_of_col[col] (-1: a zero
+// column), or col itself while col < rows when row_of_col is null.  With
+// power-of-two scales the bf16 value is the E4M3 value exactly.  Tiles of
+// 128 columns x 64 c, every dst column written; C % 8 == 0, an even ldd, 16-byte aligned
+// src rows.
+__global__ void __launch_bounds__(256) transpose_fq_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C,
+                                                           int64_t src_batch, const int32_t* __restrict__ row_of_col,
+                                                           const int32_t* __restrict__ perm, int n_cols,
+                                                           __nv_bfloat16* __restrict__ dst, int64_t ldd,
+                                                           int64_t dst_batch, bool pow2) {
+  __shared__ float tile[64][129];  // [c - c0][col - col0]
+  src += blockIdx.z * src_batch;
+  dst += blockIdx.z * dst_batch;
+  const int c0 = blockIdx.x * 64, col0 = blockIdx.y * 128, tid = threadIdx.x;
+  const int chunk = tid & 7;  // 8 columns c of the src row
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int cl = (tid >> 3) + 32 * i, col = col0 + cl;
+    int r = -1;
+    if (col < n_cols) {
+      r = row_of_col ? row_of_col[col] : (col < rows ? col : -1);
+      if (r >= 0 && perm) r = perm[r];
+    }
+    const int c = c0 + chunk * 8;
+    float f[8];
+    if (r >= 0 && r < rows && c < C) {
+      unpack8(*reinterpret_cast<const uint4*>(src + (int64_t)r * C + c), f);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) f[j] = 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) tile[chunk * 8 + j][cl] = f[j];
+  }
+  __syncthreads();
+  // a warp per dst row (8 rows per warp, two at a time): lane l holds the
+  // column pairs 2l and 64 + 2l, written as 4-byte bf16 pairs
+  const int warp = tid >> 5, lane = tid & 31;
+#pragma unroll 2
+  for (int i = 0; i < 8; ++i) {
+    const int cl = warp + 8 * i, c = c0 + cl;
+    float v[4], amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      v[2 * j] = tile[cl][2 * lane + 64 * j];
+      v[2 * j + 1] = tile[cl][2 * lane + 1 + 64 * j];
+      amax = fmaxf(amax, fmaxf(fabsf(v[2 * j]), fabsf(v[2 * j + 1])));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (c >= C) continue;
+    float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+    if (pow2) scale = pow2_ceil(scale);
+    const float inv = 1.0f / scale;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int col = col0 + 2 * lane + 64 * j;
+      if (col >= n_cols) continue;
+      const __nv_fp8x2_storage_t q =
+          __nv_cvt_float2_to_fp8x2(make_float2(v[2 * j] * inv, v[2 * j + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+      const float2 back = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(q, __NV_E4M3)));
+      __nv_bfloat16* o = dst + (int64_t)c * ldd + col;
+      if (col + 1 < n_cols) *reinterpret_cast<uint32_t*>(o) = pack_bf16x2(back.x * scale, back.y * scale);
+      else *o = __float2bfloat16_rn(back.x * scale);
+    }
+  }
+}
+
+// 1 x 128 quantisation of bf16 rows (ai.flicky.cc 3.3 item 2): the operand
+// of an FP8 GEMM whose K runs along the rows.  codes [rows, C] E4M3 and
+// scales [C/128][scale_ld] fp32 (MN-major, the layout of the GEMMs' activation
+// scales): scale = amax/448 (UE8M0: rounded up to a power of two; 1 for an
+// all-zero tile), codes = E4M3 of x * (1/scale) in fp32 with one correctly
+// rounded reciprocal per tile (the rows are intermediates known to bf16
+// accuracy).  A warp per row, a quarter warp per tile.
+__global__ void __launch_bounds__(256) quant_rows_kernel(const __nv_bfloat16* __restrict__ src, int64_t rows, int C,
+                                                         uint8_t* __restrict__ codes, float* __restrict__ scales,
+                                                         int64_t scale_ld, bool pow2) {
+  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const uint4* s4 = reinterpret_cast<const uint4*>(src + row * C);
+  const int groups = C / 128, ql = lane & 7, qw = lane >> 3;
+  for (int g0 = 0; g0 < groups; g0 += 4) {
+    const int g = g0 + qw;
+    const bool active = g < groups;
+    float f0[8], f1[8];
+    float amax = 0.0f;
+    if (active) {
+      unpack8(s4[g * 16 + 2 * ql], f0);
+      unpack8(s4[g * 16 + 2 * ql + 1], f1);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fmaxf(fabsf(f0[i]), fabsf(f1[i])));
+    }
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+    if (pow2) scale = pow2_ceil(scale);
+    const float inv = 1.0f / scale;
+    if (active) {
+      uint32_t c8[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        c8[i] = e4m3x2(f0[2 * i] * inv, f0[2 * i + 1] * inv);
+        c8[4 + i] = e4m3x2(f1[2 * i] * inv, f1[2 * i + 1] * inv);
+      }
+      reinterpret_cast<uint4*>(codes + row * C + g * 128)[ql] =
+          make_uint4(c8[0] | (c8[1] << 16), c8[2] | (c8[3] << 16), c8[4] | (c8[5] << 16), c8[6] | (c8[7] << 16));
+      if (ql == 0) scales[(int64_t)g * scale_ld + row] = scale;
+    }
+  }
+}
+
+// dst[b][c][r] = src[b][r][c] for bytes (FP8 weight codes [rows, C] per
+// expert -> [C, rows]): 64 x 64 tiles, 16-byte loads, 4-byte stores; rows and
+// C multiples of 4, 16-byte aligned rows.
+__global__ void __launch_bounds__(256) transpose_u8_kernel(const uint8_t* __restrict__ src, int rows, int C,
+                                                           int64_t batch_stride, uint8_t* __restrict__ dst) {
+  __shared__ __align__(16) uint8_t tile[64][80];  // [r - r0][c - c0]
+  src += blockIdx.z * batch_stride;
+  dst += blockIdx.z * batch_stride;
+  const int c0 = blockIdx.x * 64, r0 = blockIdx.y * 64, tid = threadIdx.x;
+  {
+    const int rl = tid >> 2, cl = (tid & 3) * 16, r = r0 + rl, c = c0 + cl;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r < rows && c < C) v = *reinterpret_cast<const uint4*>(src + (int64_t)r * C + c);
+    *reinterpret_cast<uint4*>(&tile[rl][cl]) = v;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int idx = tid + 256 * i, cl = idx >> 4, rl = (idx & 15) * 4, c = c0 + cl, r = r0 + rl;
+    if (c >= C || r >= rows) continue;
+    const uint32_t w = uint32_t(tile[rl][cl]) | (uint32_t(tile[rl + 1][cl]) << 8) |
+                       (uint32_t(tile[rl + 2][cl]) << 16) | (uint32_t(tile[rl + 3][cl]) << 24);
+    *reinterpret_cast<uint32_t*>(dst + (int64_t)c * rows + r) = w;
+  }
+}
+
+// dst[b][j][i] = src[b][i][j] for a small fp32 grid [rows, cols] per batch
+// entry (the block scales of a transposed weight).
+__global__ void transpose_f32_kernel(const float* __restrict__ src, int rows, int cols, int batch,
+                                     float* __restrict__ dst) {
+  const int64_t n = int64_t(batch) * rows * cols;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t b = i / (int64_t(rows) * cols);
+    const int rem = static_cast<int>(i - b * rows * cols), r = rem / cols, c = rem - r * cols;
+    dst[b * rows * cols + int64_t(c) * rows + r] = src[i];
+  }
+}
+
 // Gate and up values of a row in the w13 interleave: features f of block
 // f / 128 sit at columns 256 (f / 128) + f % 128 (gate) and + 128 (up).
 __device__ __forceinline__ int64_t gate_col(int f) { return 256 * (f >> 7) + (f & 127); }
 
-// 8 bf16 <-> 8 floats
-__device__ __forceinline__ void unpack8_bf16(const uint4& v, float (&f)[8]) {
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 p = __bfloat1622float2(h[i]);
-    f[2 * i] = p.x;
-    f[2 * i + 1] = p.y;
-  }
-}
+// 8 floats -> 8 bf16 (16 bytes); unpack8 (kernels.cuh) is the inverse
 __device__ __forceinline__ uint4 pack8_bf16(const float (&f)[8]) {
   return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
 }
@@ -131,8 +284,8 @@ __global__ void swiglu_fwd_kernel(const __nv_bfloat16* __restrict__ ab, int64_t 
     const int f = static_cast<int>(i - r * I8) * 8;
     const __nv_bfloat16* row = ab + r * 2 * I + gate_col(f);
     float a[8], b[8], o[8];
-    unpack8_bf16(*reinterpret_cast<const uint4*>(row), a);
-    unpack8_bf16(*reinterpret_cast<const uint4*>(row + 128), b);
+    unpack8(*reinterpret_cast<const uint4*>(row), a);
+    unpack8(*reinterpret_cast<const uint4*>(row + 128), b);
 #pragma unroll
     for (int j = 0; j < 8; ++j) o[j] = silu(a[j]) * b[j];
     *reinterpret_cast<uint4*>(h + r * I + f) = pack8_bf16(o);
@@ -152,9 +305,9 @@ __global__ void swiglu_bwd_kernel(const __nv_bfloat16* __restrict__ ab, const __
     const int f = static_cast<int>(i - r * I8) * 8;
     const int64_t ca = r * 2 * I + gate_col(f);
     float a[8], b[8], g[8], da[8], db[8];
-    unpack8_bf16(*reinterpret_cast<const uint4*>(ab + ca), a);
-    unpack8_bf16(*reinterpret_cast<const uint4*>(ab + ca + 128), b);
-    unpack8_bf16(*reinterpret_cast<const uint4*>(dh + r * I + f), g);
+    unpack8(*reinterpret_cast<const uint4*>(ab + ca), a);
+    unpack8(*reinterpret_cast<const uint4*>(ab + ca + 128), b);
+    unpack8(*reinterpret_cast<const uint4*>(dh + r * I + f), g);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const float sg = 1.0f / (1.0f + __expf(-a[j]));
@@ -209,8 +362,8 @@ __global__ void __launch_bounds__(128) combine_bwd_kernel(
       const float gj = s_g[j];
       for (int c8 = tid; c8 < d8; c8 += blockDim.x) {
         float gv[8], yv[8], o[8];
-        unpack8_bf16(reinterpret_cast<const uint4*>(Gt)[c8], gv);
-        unpack8_bf16(reinterpret_cast<const uint4*>(y + (int64_t)sl * d)[c8], yv);
+        unpack8(reinterpret_cast<const uint4*>(Gt)[c8], gv);
+        unpack8(reinterpret_cast<const uint4*>(y + (int64_t)sl * d)[c8], yv);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           o[i] = gj * gv[i];
@@ -247,11 +400,11 @@ __global__ void __launch_bounds__(128) combine_bwd_kernel(
   __syncthreads();
   for (int c8 = tid; c8 < d8; c8 += blockDim.x) {
     float acc[8];
-    unpack8_bf16(reinterpret_cast<const uint4*>(Gt)[c8], acc);
+    unpack8(reinterpret_cast<const uint4*>(Gt)[c8], acc);
     for (int j = 0; j < k; ++j) {
       if (s_e[j] < 0) continue;
       float cv[8];
-      unpack8_bf16(reinterpret_cast<const uint4*>(cent + (int64_t)s_e[j] * d)[c8], cv);
+      unpack8(reinterpret_cast<const uint4*>(cent + (int64_t)s_e[j] * d)[c8], cv);
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = fmaf(s_dz[j], cv[i], acc[i]);
     }
@@ -282,13 +435,13 @@ __global__ void __launch_bounds__(128) gather_dx_kernel(const __nv_bfloat16* __r
     for (int j = 0; j < k; ++j) {
       if (s_slot[j] < 0) continue;
       float v[8];
-      unpack8_bf16(reinterpret_cast<const uint4*>(dx + (int64_t)s_slot[j] * d)[c8], v);
+      unpack8(reinterpret_cast<const uint4*>(dx + (int64_t)s_slot[j] * d)[c8], v);
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] += v[i];
     }
     for (int s = 0; s < n_shared; ++s) {
       float v[8];
-      unpack8_bf16(reinterpret_cast<const uint4*>(dx_shared + ((int64_t)s * T + t) * d)[c8], v);
+      unpack8(reinterpret_cast<const uint4*>(dx_shared + ((int64_t)s * T + t) * d)[c8], v);
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] += v[i];
     }

@@ -726,7 +726,10 @@ namespace {
 struct BwdLayout {
   Layout f;
   size_t queue, ab, dy, dh, dab, dx, dz_row, ab_s, dh_s, dab_s, dx_s, pad_off, row_of_col, wg_r, wg_s2, wg_s13;
-  size_t xT, dyT, hT, dabT, uT, GT, hsT, dabsT, total;
+  size_t xT, dyT, hT, dabT, uT, GT, hsT, dabsT;
+  // FP8 only: bf16 h (routed, shared) and the E4M3 codes + 1 x 128 scales of
+  // the data-gradient GEMMs' activation operands
+  size_t hb, hsb, dyq, dys, dabq, dabs, Gq, Gs, dabsq, dabss, total;
   int64_t Rp, Tp;
 };
 
@@ -740,8 +743,11 @@ BwdLayout make_bwd_layout(const moe_dims& d) {
     return o;
   };
   const int64_t T = d.T, R = T * d.k, E = d.E, I = d.inter, D = d.d, Ns = d.n_shared;
-  B.Rp = (R + 64 * E + 63) / 64 * 64;  // every expert's rows padded to a multiple of 64 columns
-  B.Tp = (T + 63) / 64 * 64;
+  // every expert's rows padded to a multiple of 64 columns (FP8: 128, the
+  // token blocks of the weight-gradient operands' quantisation)
+  const int64_t gran = is_fp8(d) ? 128 : 64;
+  B.Rp = (R + gran * E + gran - 1) / gran * gran;
+  B.Tp = (T + gran - 1) / gran * gran;
   B.queue = take(16 * sizeof(int));
   B.ab = take(R * 2 * I * 2);
   B.dy = take(R * D * 2);
@@ -766,6 +772,18 @@ BwdLayout make_bwd_layout(const moe_dims& d) {
   B.GT = take(D * B.Tp * 2);
   B.hsT = take(I * Ns * B.Tp * 2);
   B.dabsT = take(2 * I * Ns * B.Tp * 2);
+  if (is_fp8(d)) {
+    B.hb = take(R * I * 2);
+    B.hsb = take(Ns * T * I * 2);
+    B.dyq = take(R * D);
+    B.dys = take(D / 128 * R * 4);
+    B.dabq = take(R * 2 * I);
+    B.dabs = take(2 * I / 128 * R * 4);
+    B.Gq = take(T * D);
+    B.Gs = take(D / 128 * T * 4);
+    B.dabsq = take(Ns * T * 2 * I);
+    B.dabss = take(2 * I / 128 * Ns * T * 4);
+  }
   B.total = off;
   return B;
 }
@@ -833,6 +851,71 @@ moe_status transpose_bf16(const void* src, int rows, int C, int64_t src_batch, c
   return launched();
 }
 
+// The FP8 weight-gradient operands: transposed gather with 1 x 128
+// quantisation along the tokens, dequantised to bf16 (transpose_fq_kernel);
+// perm (optional) maps the gathered row once more (the routed experts' u rows).
+moe_status transpose_fq(const void* src, int rows, int C, int64_t src_batch, const int32_t* row_of_col,
+                        const int32_t* perm, int64_t n_cols, void* dst, int64_t ldd, int64_t dst_batch, int batch,
+                        bool pow2, cudaStream_t st) {
+  if (n_cols <= 0 || C <= 0 || batch <= 0) return MOE_OK;
+  if (C % 8 || n_cols > INT_MAX) return MOE_ERR_UNSUPPORTED;
+  dim3 grid(static_cast<unsigned>(cdiv(C, 64)), static_cast<unsigned>(cdiv(n_cols, 128)), static_cast<unsigned>(batch));
+  transpose_fq_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, C, src_batch, row_of_col,
+                                             perm, static_cast<int>(n_cols), static_cast<__nv_bfloat16*>(dst), ldd,
+                                             dst_batch, pow2);
+  return launched();
+}
+
+// 1 x 128 quantisation of bf16 rows [rows, C] -> codes + scales [C/128][scale_ld].
+moe_status quant_rows(const void* src, int64_t rows, int C, void* codes, void* scales, int64_t scale_ld, bool pow2,
+                      cudaStream_t st) {
+  if (rows <= 0) return MOE_OK;
+  quant_rows_kernel<<<static_cast<unsigned>(cdiv(rows * 32, 256)), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(src), rows, C, static_cast<uint8_t*>(codes), static_cast<float*>(scales),
+      scale_ld, pow2);
+  return launched();
+}
+
+// One FP8 expert-GEMM launch with the bf16 epilogue: out[rows of group g] =
+// dequant(A rows) . dequant(W_g)^T, A codes [a_rows, K] with 1 x 128 scales
+// [K/128][a_scale_ld], W codes [.. , K] with N rows per group and 128 x 128
+// block scales.  table != nullptr: groups from the device tables (rows_cap
+// rows at most); else n_groups uniform groups of uni_m rows, A rows of group
+// g from g * uni_a_step, output rows from g * uni_m.
+moe_status fp8gemm_bf16(const void* w, const float* wsc, int64_t w_rows, int N, int K, const void* a,
+                        const float* asc, int64_t a_scale_ld, int64_t a_rows, void* out, int64_t out_ld, int n_groups,
+                        const GroupEntry* table, const int32_t* mt_total, const int32_t* cgroup, int64_t rows_cap,
+                        int uni_m, int uni_a_step, int* queue, int* status, cudaStream_t st) {
+  CUtensorMap ta, tb;
+  MOE_TRY(make_tmap(&ta, a, true, a_rows, K, 128));
+  MOE_TRY(make_tmap(&tb, w, true, w_rows, K, 256));
+  GemmArgs g = base_args(status);
+  g.queue = queue;
+  g.groups = table;
+  g.mt_total = mt_total;
+  g.chunk_group = cgroup;
+  g.n_groups = n_groups;
+  g.uni_m = uni_m;
+  g.uni_a_step = uni_a_step;
+  g.uni_out_step = uni_m;
+  g.N = N;
+  g.K = K;
+  g.b_rows_per_group = N;
+  g.a_rows_cap = static_cast<int32_t>(a_rows);
+  g.out = out;
+  g.out_ld = out_ld;
+  g.a_scale = asc;
+  g.a_scale_ld = a_scale_ld;
+  g.b_scale = wsc;
+  const int64_t rows = table ? rows_cap : int64_t(uni_m) * n_groups;
+#ifdef MOE_CHECK
+  g.b_rows = w_rows;
+  g.out_rows = static_cast<int32_t>(rows);
+#endif
+  const int64_t mt = table ? cdiv(rows_cap + 127 * int64_t(n_groups), 128) : int64_t(n_groups) * cdiv(uni_m, 128);
+  return launch_fp8<Epi::BF16>(ta, tb, g, mt * cdiv(N, 256), rows < 64 * int64_t(n_groups), false, st);
+}
+
 // Weight gradients of n_groups groups: out[g] [M, N] fp32 = A[:, ka..] . B[:, kb..]^T.
 // fp32 output [G][M][N] for TMA stores: boxes of 32 x 32 elements, 128-byte
 // swizzle (the layout the wgrad epilogue writes its staging boxes in).
@@ -876,6 +959,152 @@ moe_status wgrad(const void* A, int64_t a_cols, int M, const void* Bm, int64_t b
 unsigned ew_blocks(int64_t n) {  // grid of the elementwise kernels (grid-strided)
   const int64_t b = cdiv(n, 256);
   return static_cast<unsigned>(b < 148 * 16 ? (b > 0 ? b : 1) : 148 * 16);
+}
+
+// The backward pass in the FP8 scheme after the routing (idx, gate, z, the
+// token x expert mask are in the workspace): see moe_backward in moe.h.
+moe_status backward_fp8(const moe_dims& d, const BwdLayout& B, const moe_weights* w, const moe_weights_t* wt,
+                        const uint16_t* u, const uint16_t* dout, const moe_grads* gr, void* ws, cudaStream_t st) {
+  const Layout& L = B.f;
+  const int64_t T = d.T, R = T * d.k, E = d.E, I = d.inter, D = d.d, Ns = d.n_shared, I2 = 2 * I;
+  const bool pow2 = d.prec == MOE_FP8_UE8M0;
+  int* status = at<int>(ws, L.status);
+  int* queue = at<int>(ws, B.queue);
+  int32_t* idx = at<int32_t>(ws, L.idx);
+  float* gate = at<float>(ws, L.gate);
+  float* z = at<float>(ws, L.z);
+  GroupEntry* groups = at<GroupEntry>(ws, L.groups);
+  int32_t* mt_total = at<int32_t>(ws, L.mt_total);
+  int32_t* cgroup = at<int32_t>(ws, L.cgroup);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* perm = at<int32_t>(ws, L.perm);
+  int32_t* slot = at<int32_t>(ws, L.slot);
+  void* x = at<void>(ws, L.x);       // E4M3 codes of the routed rows, scales xs [d/128][R]
+  float* xs = at<float>(ws, L.xs);
+  uint8_t* uq = Ns > 0 ? at<uint8_t>(ws, L.uq) : nullptr;  // codes of u for the shared experts, uqs [d/128][T]
+  float* uqs = Ns > 0 ? at<float>(ws, L.uqs) : nullptr;
+  MOE_TRY(enqueue_dispatch(d, idx, u, at<uint32_t>(ws, L.mask), at<int32_t>(ws, L.wprefix), at<int32_t>(ws, L.cnt),
+                           offsets, groups, mt_total, cgroup, perm, slot, x, xs, uq, uqs, status, st));
+  const int Ei = static_cast<int>(E), Nsi = static_cast<int>(Ns), Ti = static_cast<int>(T);
+  void* ab = at<void>(ws, B.ab);
+  void* hb = at<void>(ws, B.hb);
+  void* hq = at<void>(ws, L.h);
+  float* hs = at<float>(ws, L.hs);
+  void* y = at<void>(ws, L.y);
+  // --- routed experts, forward: a|b (bf16), h (bf16, then E4M3 along I), y
+  MOE_TRY(fp8gemm_bf16(w->w13, w->w13_scale, E * I2, static_cast<int>(I2), static_cast<int>(D), x, xs, R, R, ab, I2,
+                       Ei, groups, mt_total, cgroup, R, 0, 0, queue + 0, status, st));
+  swiglu_fwd_kernel<<<ew_blocks(R * I / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab), R,
+                                                           static_cast<int>(I), static_cast<__nv_bfloat16*>(hb));
+  MOE_TRY(launched());
+  MOE_TRY(quant_rows(hb, R, static_cast<int>(I), hq, hs, R, pow2, st));
+  MOE_TRY(fp8gemm_bf16(w->w2, w->w2_scale, E * D, static_cast<int>(D), static_cast<int>(I), hq, hs, R, R, y, D, Ei,
+                       groups, mt_total, cgroup, R, 0, 0, queue + 1, status, st));
+  // --- combine and gates backward (fp32): dy, dz, du = G + router share
+  void* dy = at<void>(ws, B.dy);
+  float* dz_row = at<float>(ws, B.dz_row);
+  const LogitsSplit sp = logits_split(d);
+  combine_bwd_kernel<<<static_cast<unsigned>(T), 128, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(y), slot, idx, gate, z,
+      sp.splits, T * E, reinterpret_cast<const __nv_bfloat16*>(w->centroids), Ti, static_cast<int>(D), d.k, Ei, R,
+      static_cast<__nv_bfloat16*>(dy), dz_row, gr->du, status);
+  MOE_TRY(launched());
+  // --- data gradients (FP8 GEMMs on the transposed weights)
+  void* dh = at<void>(ws, B.dh);
+  void* dab = at<void>(ws, B.dab);
+  void* dx = at<void>(ws, B.dx);
+  MOE_TRY(quant_rows(dy, R, static_cast<int>(D), at<void>(ws, B.dyq), at<void>(ws, B.dys), R, pow2, st));
+  MOE_TRY(fp8gemm_bf16(wt->w2t, wt->w2t_scale, E * I, static_cast<int>(I), static_cast<int>(D), at<void>(ws, B.dyq),
+                       at<float>(ws, B.dys), R, R, dh, I, Ei, groups, mt_total, cgroup, R, 0, 0, queue + 2, status, st));
+  swiglu_bwd_kernel<<<ew_blocks(R * I / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab),
+                                                           static_cast<const __nv_bfloat16*>(dh), R,
+                                                           static_cast<int>(I), static_cast<__nv_bfloat16*>(dab));
+  MOE_TRY(launched());
+  MOE_TRY(quant_rows(dab, R, static_cast<int>(I2), at<void>(ws, B.dabq), at<void>(ws, B.dabs), R, pow2, st));
+  MOE_TRY(fp8gemm_bf16(wt->w13t, wt->w13t_scale, E * D, static_cast<int>(D), static_cast<int>(I2),
+                       at<void>(ws, B.dabq), at<float>(ws, B.dabs), R, R, dx, D, Ei, groups, mt_total, cgroup, R, 0,
+                       0, queue + 3, status, st));
+  // --- shared experts: every token, output gradient G itself
+  void* ab_s = at<void>(ws, B.ab_s);
+  void* hsb = at<void>(ws, B.hsb);
+  void* dh_s = at<void>(ws, B.dh_s);
+  void* dab_s = at<void>(ws, B.dab_s);
+  void* dx_s = at<void>(ws, B.dx_s);
+  if (Ns > 0) {
+    MOE_TRY(fp8gemm_bf16(w->ws13, w->ws13_scale, Ns * I2, static_cast<int>(I2), static_cast<int>(D), uq, uqs, T, T,
+                         ab_s, I2, Nsi, nullptr, nullptr, nullptr, 0, Ti, 0, queue + 4, status, st));
+    swiglu_fwd_kernel<<<ew_blocks(Ns * T * I / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab_s), Ns * T,
+                                                                  static_cast<int>(I), static_cast<__nv_bfloat16*>(hsb));
+    MOE_TRY(launched());
+    MOE_TRY(quant_rows(dout, T, static_cast<int>(D), at<void>(ws, B.Gq), at<void>(ws, B.Gs), T, pow2, st));
+    MOE_TRY(fp8gemm_bf16(wt->ws2t, wt->ws2t_scale, Ns * I, static_cast<int>(I), static_cast<int>(D),
+                         at<void>(ws, B.Gq), at<float>(ws, B.Gs), T, T, dh_s, I, Nsi, nullptr, nullptr, nullptr, 0, Ti,
+                         0, queue + 5, status, st));
+    swiglu_bwd_kernel<<<ew_blocks(Ns * T * I / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab_s),
+                                                                  static_cast<const __nv_bfloat16*>(dh_s), Ns * T,
+                                                                  static_cast<int>(I),
+                                                                  static_cast<__nv_bfloat16*>(dab_s));
+    MOE_TRY(launched());
+    MOE_TRY(quant_rows(dab_s, Ns * T, static_cast<int>(I2), at<void>(ws, B.dabsq), at<void>(ws, B.dabss), Ns * T,
+                       pow2, st));
+    MOE_TRY(fp8gemm_bf16(wt->ws13t, wt->ws13t_scale, Ns * D, static_cast<int>(D), static_cast<int>(I2),
+                         at<void>(ws, B.dabsq), at<float>(ws, B.dabss), Ns * T, Ns * T, dx_s, D, Nsi, nullptr,
+                         nullptr, nullptr, 0, Ti, Ti, queue + 6, status, st));
+  }
+  gather_dx_kernel<<<static_cast<unsigned>(T), 128, 0, st>>>(static_cast<const __nv_bfloat16*>(dx), slot, d.k, R,
+                                                              static_cast<const __nv_bfloat16*>(dx_s), Nsi, Ti,
+                                                              static_cast<int>(D), gr->du);
+  MOE_TRY(launched());
+  dcent_kernel<<<dim3(static_cast<unsigned>(E), static_cast<unsigned>(cdiv(D, 256))), 256, 0, st>>>(
+      dz_row, perm, offsets, reinterpret_cast<const __nv_bfloat16*>(u), static_cast<int>(D), gr->dcentroids);
+  MOE_TRY(launched());
+  // --- weight gradients: operands quantised along the tokens (128-token
+  // blocks from each expert's first token), products on the bf16 path
+  int32_t* pad_off = at<int32_t>(ws, B.pad_off);
+  int32_t* row_of_col = at<int32_t>(ws, B.row_of_col);
+  WgradGroup* wg_r = at<WgradGroup>(ws, B.wg_r);
+  pad_plan_kernel<<<1, 1024, 0, st>>>(offsets, Ei, static_cast<int>(B.Rp), 128, pad_off, row_of_col, status);
+  MOE_TRY(launched());
+  wgrad_table_kernel<<<static_cast<unsigned>(cdiv(E, 256)), 256, 0, st>>>(pad_off, Ei, wg_r);
+  MOE_TRY(launched());
+  void* xT = at<void>(ws, B.xT);
+  void* dyT = at<void>(ws, B.dyT);
+  void* hT = at<void>(ws, B.hT);
+  void* dabT = at<void>(ws, B.dabT);
+  MOE_TRY(transpose_fq(u, Ti, static_cast<int>(D), 0, row_of_col, perm, B.Rp, xT, B.Rp, 0, 1, pow2, st));
+  MOE_TRY(transpose_fq(dy, static_cast<int>(R), static_cast<int>(D), 0, row_of_col, nullptr, B.Rp, dyT, B.Rp, 0, 1,
+                       pow2, st));
+  MOE_TRY(transpose_fq(hb, static_cast<int>(R), static_cast<int>(I), 0, row_of_col, nullptr, B.Rp, hT, B.Rp, 0, 1,
+                       pow2, st));
+  MOE_TRY(transpose_fq(dab, static_cast<int>(R), static_cast<int>(I2), 0, row_of_col, nullptr, B.Rp, dabT, B.Rp, 0,
+                       1, pow2, st));
+  MOE_TRY(wgrad(dyT, B.Rp, static_cast<int>(D), hT, B.Rp, static_cast<int>(I), wg_r, Ei, gr->dw2, queue + 8, status,
+                st));
+  MOE_TRY(wgrad(dabT, B.Rp, static_cast<int>(I2), xT, B.Rp, static_cast<int>(D), wg_r, Ei, gr->dw13, queue + 9,
+                status, st));
+  if (Ns > 0) {
+    void* uT = at<void>(ws, B.uT);
+    void* GT = at<void>(ws, B.GT);
+    void* hsT = at<void>(ws, B.hsT);
+    void* dabsT = at<void>(ws, B.dabsT);
+    const int Tp = static_cast<int>(B.Tp);
+    MOE_TRY(transpose_fq(u, Ti, static_cast<int>(D), 0, nullptr, nullptr, Tp, uT, Tp, 0, 1, pow2, st));
+    MOE_TRY(transpose_fq(dout, Ti, static_cast<int>(D), 0, nullptr, nullptr, Tp, GT, Tp, 0, 1, pow2, st));
+    MOE_TRY(transpose_fq(hsb, Ti, static_cast<int>(I), T * I, nullptr, nullptr, Tp, hsT, Ns * Tp, Tp, Nsi, pow2, st));
+    MOE_TRY(transpose_fq(dab_s, Ti, static_cast<int>(I2), T * I2, nullptr, nullptr, Tp, dabsT, Ns * Tp, Tp, Nsi, pow2,
+                         st));
+    WgradGroup* wg_s2 = at<WgradGroup>(ws, B.wg_s2);
+    WgradGroup* wg_s13 = at<WgradGroup>(ws, B.wg_s13);
+    wgrad_strided_table_kernel<<<1, 256, 0, st>>>(Nsi, 0, Tp, Tp, wg_s2);   // A = G^T, B = h_s^T
+    MOE_TRY(launched());
+    wgrad_strided_table_kernel<<<1, 256, 0, st>>>(Nsi, Tp, 0, Tp, wg_s13);  // A = dab_s^T, B = u^T
+    MOE_TRY(launched());
+    MOE_TRY(wgrad(GT, Tp, static_cast<int>(D), hsT, Ns * Tp, static_cast<int>(I), wg_s2, Nsi, gr->dws2, queue + 10,
+                  status, st));
+    MOE_TRY(wgrad(dabsT, Ns * Tp, static_cast<int>(I2), uT, Tp, static_cast<int>(D), wg_s13, Nsi, gr->dws13,
+                  queue + 11, status, st));
+  }
+  return MOE_OK;
 }
 
 }  // namespace
@@ -928,7 +1157,6 @@ moe_status moe_forward_replicated(const moe_dims* dims, const moe_weights* w, co
 moe_status moe_backward_workspace_size(const moe_dims* dims, size_t* bytes) {
   MOE_TRY(check_dims(dims));
   if (!bytes) return MOE_ERR_INVALID_ARG;
-  if (dims->prec != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   *bytes = make_bwd_layout(*dims).total;
   return MOE_OK;
 }
@@ -943,14 +1171,39 @@ moe_status moe_transpose_expert_weights(int32_t n_experts, int32_t inter, int32_
   return transpose_bf16(w2, d, inter, int64_t(d) * inter, nullptr, d, w2t, d, int64_t(d) * inter, n_experts, st);
 }
 
+moe_status moe_transpose_expert_weights_fp8(int32_t n_experts, int32_t inter, int32_t d, const uint8_t* w13,
+                                            const float* w13_scale, const uint8_t* w2, const float* w2_scale,
+                                            uint8_t* w13t, float* w13t_scale, uint8_t* w2t, float* w2t_scale,
+                                            void* stream) {
+  if (n_experts <= 0 || n_experts > 65535 || inter <= 0 || d <= 0 || inter % 128 || d % 128) return MOE_ERR_INVALID_ARG;
+  if (!w13 || !w2 || !w13t || !w2t || !w13_scale || !w2_scale || !w13t_scale || !w2t_scale)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w13) || !aligned16(w2) || !aligned16(w13t) || !aligned16(w2t)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int I2 = 2 * inter;
+  transpose_u8_kernel<<<dim3(static_cast<unsigned>(d / 64), static_cast<unsigned>(I2 / 64),
+                             static_cast<unsigned>(n_experts)), 256, 0, st>>>(w13, I2, d, int64_t(I2) * d, w13t);
+  MOE_TRY(launched());
+  transpose_u8_kernel<<<dim3(static_cast<unsigned>(inter / 64), static_cast<unsigned>(d / 64),
+                             static_cast<unsigned>(n_experts)), 256, 0, st>>>(w2, d, inter, int64_t(d) * inter, w2t);
+  MOE_TRY(launched());
+  transpose_f32_kernel<<<ew_blocks(int64_t(n_experts) * (I2 / 128) * (d / 128)), 256, 0, st>>>(
+      w13_scale, I2 / 128, d / 128, n_experts, w13t_scale);
+  MOE_TRY(launched());
+  transpose_f32_kernel<<<ew_blocks(int64_t(n_experts) * (d / 128) * (inter / 128)), 256, 0, st>>>(
+      w2_scale, d / 128, inter / 128, n_experts, w2t_scale);
+  return launched();
+}
+
 moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_weights_t* wt, const uint16_t* u,
                         const float* bias, const uint16_t* dout, const moe_grads* gr, void* ws, size_t ws_bytes,
                         void* stream) {
   MOE_TRY(check_dims(dims));
-  if (dims->prec != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   MOE_TRY(check_weights(*dims, w));
   const moe_dims& d = *dims;
   if (!wt || !wt->w13t || !wt->w2t || (d.n_shared > 0 && (!wt->ws13t || !wt->ws2t))) return MOE_ERR_INVALID_ARG;
+  if (is_fp8(d) && (!wt->w13t_scale || !wt->w2t_scale || (d.n_shared > 0 && (!wt->ws13t_scale || !wt->ws2t_scale))))
+    return MOE_ERR_INVALID_ARG;
   if (!gr || !gr->du || !gr->dcentroids || !gr->dw13 || !gr->dw2 || (d.n_shared > 0 && (!gr->dws13 || !gr->dws2)))
     return MOE_ERR_INVALID_ARG;
   // vector stores of du, TMA stores of the weight gradients
@@ -986,6 +1239,7 @@ moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_we
   float* gate = at<float>(ws, L.gate);
   float* z = at<float>(ws, L.z);
   MOE_TRY(enqueue_route(d, u, w->centroids, bias, idx, gate, at<int32_t>(ws, L.counts), mask, z, status, st));
+  if (is_fp8(d)) return backward_fp8(d, B, w, wt, u, dout, gr, ws, st);
   GroupEntry* groups = at<GroupEntry>(ws, L.groups);
   int32_t* mt_total = at<int32_t>(ws, L.mt_total);
   int32_t* cgroup = at<int32_t>(ws, L.cgroup);
@@ -1063,7 +1317,8 @@ moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_we
   int32_t* pad_off = at<int32_t>(ws, B.pad_off);
   int32_t* row_of_col = at<int32_t>(ws, B.row_of_col);
   WgradGroup* wg_r = at<WgradGroup>(ws, B.wg_r);
-  pad_plan_kernel<<<1, 1024, 0, st>>>(offsets, static_cast<int>(E), static_cast<int>(B.Rp), pad_off, row_of_col, status);
+  pad_plan_kernel<<<1, 1024, 0, st>>>(offsets, static_cast<int>(E), static_cast<int>(B.Rp), 64, pad_off, row_of_col,
+                                      status);
   MOE_TRY(launched());
   wgrad_table_kernel<<<static_cast<unsigned>(cdiv(E, 256)), 256, 0, st>>>(pad_off, static_cast<int>(E), wg_r);
   MOE_TRY(launched());

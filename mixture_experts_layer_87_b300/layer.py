@@ -100,24 +100,40 @@ class MoELayer:
     def status(self) -> int:
         return capi.moe_read_device_status(self.ws)
 
-    # ------------------------------------------------------------ backward (bf16)
+    # ------------------------------------------------------------ backward
     def prepare_backward(self) -> None:
-        """Transposed copies of the expert weights and the backward workspace."""
-        assert not self.fp8, "the backward pass is built for bf16 layers"
+        """Transposed copies of the expert weights (FP8: their codes and block
+        scales) and the backward workspace."""
         dev, I, d = self.device, self.inter, self.d
         ns = max(self.n_shared, 1)
-        self.w13t = torch.empty((self.E, d, 2 * I), dtype=torch.bfloat16, device=dev)
-        self.w2t = torch.empty((self.E, I, d), dtype=torch.bfloat16, device=dev)
-        self.ws13t = torch.empty((ns, d, 2 * I), dtype=torch.bfloat16, device=dev)
-        self.ws2t = torch.empty((ns, I, d), dtype=torch.bfloat16, device=dev)
-        capi.moe_transpose_expert_weights(self.E, I, d, self.w13, self.w2, self.w13t, self.w2t)
-        if self.n_shared:
-            capi.moe_transpose_expert_weights(self.n_shared, I, d, self.ws13, self.ws2, self.ws13t, self.ws2t)
+        wt = torch.uint8 if self.fp8 else torch.bfloat16
+        self.w13t = torch.empty((self.E, d, 2 * I), dtype=wt, device=dev)
+        self.w2t = torch.empty((self.E, I, d), dtype=wt, device=dev)
+        self.ws13t = torch.empty((ns, d, 2 * I), dtype=wt, device=dev)
+        self.ws2t = torch.empty((ns, I, d), dtype=wt, device=dev)
+        if self.fp8:
+            f = torch.float32
+            self.w13t_scale = torch.empty((self.E, d // 128, 2 * I // 128), dtype=f, device=dev)
+            self.w2t_scale = torch.empty((self.E, I // 128, d // 128), dtype=f, device=dev)
+            self.ws13t_scale = torch.empty((ns, d // 128, 2 * I // 128), dtype=f, device=dev)
+            self.ws2t_scale = torch.empty((ns, I // 128, d // 128), dtype=f, device=dev)
+            capi.moe_transpose_expert_weights_fp8(self.E, I, d, self.w13, self.w13_scale, self.w2, self.w2_scale,
+                                                  self.w13t, self.w13t_scale, self.w2t, self.w2t_scale)
+            if self.n_shared:
+                capi.moe_transpose_expert_weights_fp8(self.n_shared, I, d, self.ws13, self.ws13_scale, self.ws2,
+                                                      self.ws2_scale, self.ws13t, self.ws13t_scale, self.ws2t,
+                                                      self.ws2t_scale)
+        else:
+            self.w13t_scale = self.w2t_scale = self.ws13t_scale = self.ws2t_scale = None
+            capi.moe_transpose_expert_weights(self.E, I, d, self.w13, self.w2, self.w13t, self.w2t)
+            if self.n_shared:
+                capi.moe_transpose_expert_weights(self.n_shared, I, d, self.ws13, self.ws2, self.ws13t, self.ws2t)
         self.ws_bwd = torch.empty(capi.moe_backward_workspace_size(self.dims), dtype=torch.uint8, device=dev)
 
     def backward(self, u: torch.Tensor, bias: torch.Tensor, dout: torch.Tensor, stream=None) -> dict:
         """Gradients (fp32) of the layer for dL/dh' = dout: du, dcentroids,
-        dw13/dw2 (routed, in the w13/w2 layouts) and dws13/dws2 (shared)."""
+        dw13/dw2 (routed, in the w13/w2 layouts) and dws13/dws2 (shared); for
+        an FP8 layer in the FP8 scheme of moe_backward."""
         if not hasattr(self, "ws_bwd"):
             self.prepare_backward()
         dev, I, d, f = self.device, self.inter, self.d, torch.float32
@@ -127,7 +143,9 @@ class MoELayer:
                  dw2=torch.empty((self.E, d, I), dtype=f, device=dev),
                  dws13=torch.empty((ns, 2 * I, d), dtype=f, device=dev),
                  dws2=torch.empty((ns, d, I), dtype=f, device=dev))
-        wt = capi.moe_weights_t(self.w13t.data_ptr(), self.w2t.data_ptr(), self.ws13t.data_ptr(), self.ws2t.data_ptr())
+        ptr = lambda t: t.data_ptr() if t is not None else None
+        wt = capi.moe_weights_t(ptr(self.w13t), ptr(self.w2t), ptr(self.ws13t), ptr(self.ws2t), ptr(self.w13t_scale),
+                                ptr(self.w2t_scale), ptr(self.ws13t_scale), ptr(self.ws2t_scale))
         gr = capi.moe_grads(*(g[k].data_ptr() for k in ("du", "dcentroids", "dw13", "dw2", "dws13", "dws2")))
         capi.moe_backward(self.dims, self.weights(), wt, u, bias, dout, gr, self.ws_bwd, stream)
         return g

@@ -55,7 +55,7 @@ def _load():
         lib.oracle_e4m3_decode.restype = ctypes.c_double
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
-        lib.oracle_quant_1x128.argtypes = [i64, i32, vp, vp, vp, i32]
+        lib.oracle_quant_1x128.argtypes = [i64, i32, vp, vp, vp, i32, i32]
         lib.oracle_quant_128x128.argtypes = [i64, i32, vp, vp, vp, i32]
         lib.oracle_swiglu.argtypes = [i64, i32, i32, vp, vp, vp, vp, i32, vp]
         lib.oracle_bias_update.argtypes = [i32, i64, i32, vp, f32, vp]
@@ -159,15 +159,17 @@ def e4m3_decode(q: np.ndarray) -> np.ndarray:
     return table[flat].reshape(np.shape(q))
 
 
-def quant_1x128(x: np.ndarray, pow2: bool = False):
+def quant_1x128(x: np.ndarray, pow2: bool = False, recip: bool = False):
     """1 x 128 activation tiles along the last axis: (codes uint8, scales fp32 [rows, cols/128]).
-    pow2: UE8M0 scales (amax/448 rounded up to a power of two)."""
+    pow2: UE8M0 scales (amax/448 rounded up to a power of two).  recip: codes
+    from x * (1/scale) in fp32 (one correctly rounded reciprocal per tile)
+    instead of x / scale."""
     x = _c(x, np.float64)
     rows, cols = x.shape
     assert cols % 128 == 0
     q = np.empty((rows, cols), np.uint8)
     s = np.empty((rows, cols // 128), np.float32)
-    _load().oracle_quant_1x128(rows, cols, x.ctypes.data, q.ctypes.data, s.ctypes.data, int(pow2))
+    _load().oracle_quant_1x128(rows, cols, x.ctypes.data, q.ctypes.data, s.ctypes.data, int(pow2), int(recip))
     return q, s
 
 
@@ -191,8 +193,8 @@ def dequant_128x128(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     return e4m3_decode(q) * np.repeat(np.repeat(s.astype(np.float64), 128, axis=0), 128, axis=1)
 
 
-def fp8_roundtrip_1x128(x: np.ndarray, pow2: bool = False) -> np.ndarray:
-    return dequant_1x128(*quant_1x128(x, pow2))
+def fp8_roundtrip_1x128(x: np.ndarray, pow2: bool = False, recip: bool = False) -> np.ndarray:
+    return dequant_1x128(*quant_1x128(x, pow2, recip))
 
 
 def fp8_roundtrip_128x128(w: np.ndarray, pow2: bool = False) -> np.ndarray:

@@ -37,6 +37,19 @@ the unquantised activations.  The quantisation is straight-through: the
 gradient of Q(x) is taken as that of x.  The router (affinities, gates,
 centroid gradient) stays in high precision (item 1).  Products of the
 dequantised operands are exact (fp64).
+
+The codes of the quantised intermediates (h before the down product, dy
+and [da db] before the data-gradient products, and every weight-gradient
+operand) are taken from x * (1/s), one correctly rounded fp32 reciprocal per
+tile: these values are known only to the kernels' accuracy, and a product
+costs the kernels far less than a division.  The codes of u in the forward
+are taken from u / s, as in the forward's gather.
+
+act_bf16=True: every intermediate the kernels keep in bf16 is rounded to
+bf16 here too (a and b, h, y, dy, dh, da and db, dx, and the dequantised
+weight-gradient operands), so that the floats that decide the E4M3 codes
+are taken in the kernels' precision; without it the intermediates are fp64.
+Rounding: to fp32, then to bf16, both round-to-nearest-even (round_bf16).
 """
 from __future__ import annotations
 
@@ -49,20 +62,34 @@ def _sigmoid(a):
     return 1.0 / (1.0 + np.exp(-a))
 
 
-def swiglu_backward(x, w1, w3, w2, dy):
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """fp64 -> fp32 -> bf16 (round-to-nearest-even each time) -> fp64, for
+    finite values: the bf16 value a kernel stores for an fp32 result."""
+    b = np.ascontiguousarray(np.asarray(x, np.float64).astype(np.float32)).view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000
+    return b.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def _identity(x):
+    return x
+
+
+def swiglu_backward(x, w1, w3, w2, dy, rb=_identity):
     """One SwiGLU expert y = W2 (SiLU(W1 x) * (W3 x)) on rows x [n, d]:
     returns (dx [n, d], dW1 [I, d], dW3 [I, d], dW2 [d, I], y [n, d]) for the
     output gradient dy [n, d].  With a = W1 x, b = W3 x, sg = sigmoid(a):
-    h = a sg b, dh = dy W2, da = dh b sg (1 + a (1 - sg)), db = dh a sg."""
-    a = x @ w1.T
-    b = x @ w3.T
+    h = a sg b, dh = dy W2, da = dh b sg (1 + a (1 - sg)), db = dh a sg.
+    rb rounds the stored intermediates (identity, or round_bf16)."""
+    a = rb(x @ w1.T)
+    b = rb(x @ w3.T)
     sg = _sigmoid(a)
-    h = a * sg * b
-    y = h @ w2.T
-    dh = dy @ w2
-    da = dh * b * sg * (1.0 + a * (1.0 - sg))
-    db = dh * a * sg
-    dx = da @ w1 + db @ w3
+    h = rb(a * sg * b)
+    y = rb(h @ w2.T)
+    dy = rb(dy)
+    dh = rb(dy @ w2)
+    da = rb(dh * b * sg * (1.0 + a * (1.0 - sg)))
+    db = rb(dh * a * sg)
+    dx = rb(da @ w1 + db @ w3)
     return dx, da.T @ x, db.T @ x, dy.T @ h, y
 
 
@@ -73,38 +100,40 @@ def _q_tok(m: np.ndarray, pow2: bool) -> np.ndarray:
     n_pad = -(-n // 128) * 128
     t = np.zeros((C, n_pad))
     t[:, :n] = m.T
-    return fp8_roundtrip_1x128(t, pow2)[:, :n].T
+    return fp8_roundtrip_1x128(t, pow2, recip=True)[:, :n].T
 
 
-def _expert_backward_fp8(x, w1, w3, w2, dy, pow2):
+def _expert_backward_fp8(x, w1, w3, w2, dy, pow2, rb=_identity):
     """swiglu_backward in the FP8 scheme (module docstring): x [n, d] the
     unquantised input rows, w* the unquantised weights, dy [n, d]."""
-    q_row = lambda m: fp8_roundtrip_1x128(m, pow2)
+    q_row = lambda m: fp8_roundtrip_1x128(m, pow2, recip=True)
     w1q, w3q, w2q = (fp8_roundtrip_128x128(w, pow2) for w in (w1, w3, w2))
-    xq = q_row(x)
-    a = xq @ w1q.T
-    b = xq @ w3q.T
+    xq = fp8_roundtrip_1x128(x, pow2)
+    a = rb(xq @ w1q.T)
+    b = rb(xq @ w3q.T)
     sg = _sigmoid(a)
-    h = a * sg * b
-    y = q_row(h) @ w2q.T
-    dh = q_row(dy) @ w2q
-    da = dh * b * sg * (1.0 + a * (1.0 - sg))
-    db = dh * a * sg
-    dx = q_row(da) @ w1q + q_row(db) @ w3q
-    ut = _q_tok(x, pow2)
-    dyt, ht, dat, dbt = (_q_tok(m, pow2) for m in (dy, h, da, db))
+    h = rb(a * sg * b)
+    y = rb(q_row(h) @ w2q.T)
+    dy = rb(dy)
+    dh = rb(q_row(dy) @ w2q)
+    da = rb(dh * b * sg * (1.0 + a * (1.0 - sg)))
+    db = rb(dh * a * sg)
+    dx = rb(q_row(da) @ w1q + q_row(db) @ w3q)
+    ut = rb(_q_tok(x, pow2))
+    dyt, ht, dat, dbt = (rb(_q_tok(m, pow2)) for m in (dy, h, da, db))
     return dx, dat.T @ ut, dbt.T @ ut, dyt.T @ ht, y
 
 
 def layer_backward(u_bits, cent_bits, idx, G, routed_weights, shared_weights, n_shared: int, E: int,
-                   fp8=False) -> dict:
+                   fp8=False, act_bf16: bool = False) -> dict:
     """Gradients of the layer for dL/dh' = G [T, d], the selection idx [T, k]
     held fixed.  routed_weights(e) / shared_weights(s) return bf16 bit patterns
     (W1, W3, W2).  Returns dict(du [T, d], dcent [E, d], dw_routed {e: (dW1,
     dW3, dW2)} for every selected expert, dw_shared [(dW1, dW3, dW2)] per
     shared expert, gate [T, k], dgate [T, k]).  fp8: False, True (amax/448
     scales) or "ue8m0" (power-of-two scales): the FP8 scheme of the module
-    docstring, whose forward is that of oracle.layer_output(fp8=...)."""
+    docstring, whose forward is that of oracle.layer_output(fp8=...).
+    act_bf16: the kernels' bf16 intermediates (module docstring)."""
     x = bf16_to_f64(u_bits)
     cent = bf16_to_f64(cent_bits)
     G = np.asarray(G, np.float64)
@@ -112,12 +141,13 @@ def layer_backward(u_bits, cent_bits, idx, G, routed_weights, shared_weights, n_
     k = idx.shape[1]
     idx = np.asarray(idx, np.int64)
     pow2 = fp8 == "ue8m0"
+    rb = round_bf16 if act_bf16 else _identity
 
     def expert(xr, ws, dy):
         w1, w3, w2 = (bf16_to_f64(w) for w in ws)
         if fp8:
-            return _expert_backward_fp8(xr, w1, w3, w2, dy, pow2)
-        return swiglu_backward(xr, w1, w3, w2, dy)
+            return _expert_backward_fp8(xr, w1, w3, w2, dy, pow2, rb)
+        return swiglu_backward(xr, w1, w3, w2, dy, rb)
 
     s_sel = _sigmoid(np.einsum("td,tjd->tj", x, cent[idx]))
     S = s_sel.sum(1, keepdims=True)

@@ -104,11 +104,13 @@ def pow2_at_least(s: np.ndarray) -> np.ndarray:
     return np.where(m == 0.5, s, np.ldexp(np.float32(1.0), e)).astype(np.float32)
 
 
-def quant_dequant(x: np.ndarray, group_rows: int, group_cols: int, pow2: bool = False) -> np.ndarray:
+def quant_dequant(x: np.ndarray, group_rows: int, group_cols: int, pow2: bool = False,
+                  recip: bool = False) -> np.ndarray:
     """Quantise x [R, C] in groups of group_rows x group_cols elements and
     return the dequantised values: scale = amax / 448 in fp32 (1 for an
     all-zero group) -- rounded up to a power of two for UE8M0 scales (pow2) --,
-    element = nearest E4M3 of (x / scale) taken in fp32, times scale."""
+    element = nearest E4M3 of (x / scale) taken in fp32 -- or, recip, of
+    x * (1 / scale) with both operations in fp32 --, times scale."""
     x = np.asarray(x, np.float64)
     R, C = x.shape
     g = x.reshape(R // group_rows, group_rows, C // group_cols, group_cols)
@@ -116,7 +118,10 @@ def quant_dequant(x: np.ndarray, group_rows: int, group_cols: int, pow2: bool = 
     scale = np.where(amax > 0, amax.astype(np.float32) / np.float32(448.0), np.float32(1.0)).astype(np.float32)
     if pow2:
         scale = pow2_at_least(scale)
-    ratio = (g.astype(np.float32) / scale).astype(np.float64)
+    if recip:
+        ratio = (g.astype(np.float32) * (np.float32(1.0) / scale).astype(np.float32)).astype(np.float64)
+    else:
+        ratio = (g.astype(np.float32) / scale).astype(np.float64)
     return (e4m3_round(ratio) * scale.astype(np.float64)).reshape(R, C)
 
 

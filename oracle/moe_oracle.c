@@ -193,11 +193,16 @@ static float scale_of(double amax, int pow2) { return pow2 ? group_scale_pow2(am
 /* Code of one element: x / scale rounded to fp32 (the kernels' precision), then E4M3. */
 static uint8_t quant_elem(double x, float scale) { return oracle_e4m3_encode((double)((float)x / scale)); }
 
+/* The same from x * (1 / scale): the fp32 reciprocal of the tile's scale
+ * (correctly rounded), then the fp32 product, then E4M3. */
+static uint8_t quant_elem_recip(double x, float inv) { return oracle_e4m3_encode((double)((float)x * inv)); }
+
 /*
  * Activation tiles 1 x 128 (ai.flicky.cc 3.3 item 2): row r, columns
- * [128g, 128g+128) share scale[r * G + g], G = cols / 128.
+ * [128g, 128g+128) share scale[r * G + g], G = cols / 128.  recip != 0: codes
+ * from x * (1/scale) (quant_elem_recip) instead of x / scale.
  */
-void oracle_quant_1x128(int64_t rows, int cols, const double* x, uint8_t* q, float* scale, int pow2) {
+void oracle_quant_1x128(int64_t rows, int cols, const double* x, uint8_t* q, float* scale, int pow2, int recip) {
   const int G = cols / 128;
 #pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < rows; ++r)
@@ -206,7 +211,9 @@ void oracle_quant_1x128(int64_t rows, int cols, const double* x, uint8_t* q, flo
       for (int c = 128 * g; c < 128 * g + 128; ++c) amax = fmax(amax, fabs(x[r * cols + c]));
       float s = scale_of(amax, pow2);
       scale[r * G + g] = s;
-      for (int c = 128 * g; c < 128 * g + 128; ++c) q[r * cols + c] = quant_elem(x[r * cols + c], s);
+      const float inv = 1.0f / s;
+      for (int c = 128 * g; c < 128 * g + 128; ++c)
+        q[r * cols + c] = recip ? quant_elem_recip(x[r * cols + c], inv) : quant_elem(x[r * cols + c], s);
     }
 }
 

@@ -123,15 +123,24 @@ def test_range_checked_build_exports_the_same_symbols():
     assert b"range-checked" in L.moe_status_string(7)
 
 
-def test_backward_rejects_fp8_and_null_arguments(lib):
-    n = ctypes.c_size_t(0)
-    d8 = _dims(prec="fp8")
-    assert lib.moe_backward_workspace_size(ctypes.byref(d8), ctypes.byref(n)) == 2     # bf16 only
-    dm = _dims()
+def test_backward_workspace_and_argument_errors(lib):
+    dm, d8 = _dims(), _dims(prec="fp8")
     need = capi.moe_backward_workspace_size(dm)
     assert need > capi.moe_workspace_size(dm)
+    # FP8: the E4M3 operands of the data-gradient GEMMs on top of the bf16 activations
+    assert capi.moe_backward_workspace_size(d8) > capi.moe_workspace_size(d8)
     fake = 1 << 20
     w, wt, gr = capi.moe_weights(), capi.moe_weights_t(), capi.moe_grads()
     assert lib.moe_backward(ctypes.byref(dm), ctypes.byref(w), ctypes.byref(wt), fake, fake, fake, ctypes.byref(gr),
                             fake, need, None) == 1
+    # FP8 without the transposed weights' block scales
+    w8 = capi.moe_weights(fake, fake, fake, fake, fake, fake, fake, fake, fake)
+    wt8 = capi.moe_weights_t(fake, fake, fake, fake, None, None, None, None)
+    gr8 = capi.moe_grads(fake, fake, fake, fake, fake, fake)
+    assert lib.moe_backward(ctypes.byref(d8), ctypes.byref(w8), ctypes.byref(wt8), fake, fake, fake, ctypes.byref(gr8),
+                            fake, capi.moe_backward_workspace_size(d8), None) == 1
+    assert lib.moe_transpose_expert_weights_fp8(2, 100, 128, fake, fake, fake, fake, fake, fake, fake, fake,
+                                                None) == 1                                  # I % 128
+    assert lib.moe_transpose_expert_weights_fp8(2, 128, 128, fake, None, fake, fake, fake, fake, fake, fake,
+                                                None) == 1                                  # no scales
     assert lib.moe_transpose_expert_weights(2, 100, 128, fake, fake, fake, fake, None) == 1       # I % 128

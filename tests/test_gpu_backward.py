@@ -1,19 +1,34 @@
-"""The backward pass on the GPU (moe_backward, bf16) against the fp64 backward
-oracle (oracle/backward.py, itself pinned to autograd and finite differences),
-with the GPU's own selection held fixed on both sides.
+"""The backward pass on the GPU (moe_backward, bf16 and FP8) against the
+backward oracle (oracle/backward.py, pinned to autograd statements and finite
+differences), with the GPU's own selection held fixed on both sides.
 
-Tolerances.  The pass keeps its activations in bf16 as the forward does (a,
-b, h, y, dy, dh, da/db, dx: each rounded to 8 significant bits, 2^-9
-relative), and a gradient goes through up to four of those roundings:
-  * data gradients (du, dcentroids): max|err| / rms(ref) <= 5e-2 -- a few
-    roundings at the largest elements (max/rms ~ 5);
-  * weight gradients: ||err|| / ||ref|| (Frobenius) <= 2e-2.  Their elements
-    are sums over an expert's few tokens of products of two activations, so
-    their distribution is heavy-tailed and max|err|/rms measures the tail, not
-    the arithmetic; four roundings of 2^-9/sqrt(3) rms each give ~0.5% in norm.
-  * and the arithmetic itself: dW2 of the first experts against the same
-    product replayed from the bf16-rounded a, b, h and dy (fp64):
-    ||err|| / ||ref|| <= 1e-3 (the GPU accumulates in fp32)."""
+Two oracle references per case:
+
+1. The kernels' precision (act_bf16=True): the oracle rounds to bf16 every
+   intermediate the kernels keep in bf16 (a, b, h, y, dy, dh, da/db, dx and
+   the dequantised weight-gradient operands), so that every E4M3 code is
+   decided from the same value on both sides.  What is left is the order of
+   the fp32 sums against fp64 (~1e-6 relative), which moves a bf16 rounding
+   in about one value in 4000 by one step (2^-8 of that value).  du sums k + 1
+   bf16 dx rows whose elements reach a few times rms(du), so a moved rounding
+   there is up to ~1.5e-2 of rms(du): data gradients max|err| / rms(ref) <=
+   2e-2; weight gradients (fp32 sums of many such values, compared in norm)
+   relative Frobenius norm <= 5e-3.
+2. The exact arithmetic (fp64 intermediates).  bf16: every intermediate
+   rounded to 8 significant bits (2^-9 relative), a gradient through up to
+   four such roundings: data gradients max|err| / rms <= 5e-2 (a few roundings
+   at the largest elements, max/rms ~ 5), weight gradients Frobenius <= 2e-2
+   (their heavy-tailed elements make max/rms measure the tail).  FP8: on top
+   of that, where a bf16 intermediate lies within its rounding of a midpoint
+   between two E4M3 values its code differs from the exact one by a step
+   (2^-3 to 2^-4 of the element): a few percent of the codes, in up to three
+   quantised operands in series, about 2% rms each in a K-long product:
+   data gradients max|err| / rms <= 1.5e-1, weight gradients Frobenius <= 5e-2.
+
+And the weight-gradient arithmetic itself: dW2 of the first experts against
+the same product replayed from bf16-rounded a, b, h and dy (fp64; FP8: the
+operands quantised along the tokens, each dequantised value rounded to bf16):
+relative Frobenius norm <= 1e-3 (the GPU accumulates in fp32)."""
 import numpy as np
 import pytest
 import torch
@@ -26,8 +41,9 @@ from parity import HostLayer, rel_err
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-BWD_TOL = 5e-2      # data gradients, max|err| / rms(ref)
-WG_TOL = 2e-2       # weight gradients, relative Frobenius norm
+KP_TOL = 2e-2       # against the kernels' precision: data gradients, max|err| / rms(ref)
+KP_WG_TOL = 5e-3    # against the kernels' precision: weight gradients, relative Frobenius norm
+EXACT_TOL = {False: (5e-2, 2e-2), True: (1.5e-1, 5e-2)}   # against fp64 intermediates, bf16 / FP8
 REPLAY_TOL = 1e-3   # dW2 against the bf16-operand replay, relative Frobenius norm
 
 
@@ -39,9 +55,27 @@ def _bf16(a):
     return torch.from_numpy(np.asarray(a, np.float64)).float().to(torch.bfloat16).double().numpy()
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "mid"])
+def _interleave13(dw1, dw3, I, d):
+    # w13 interleave: rows [256j, 256j+128) of W1 block j, [256j+128, 256j+256) of W3 block j
+    return np.stack([dw1.reshape(I // 128, 128, d), dw3.reshape(I // 128, 128, d)], 1).reshape(2 * I, d)
+
+
+def _errors(got, ref, cfg):
+    errs = {"du": rel_err(got["du"], ref["du"]), "dcentroids": rel_err(got["dcentroids"], ref["dcent"])}
+    werr = {}
+    for e, (dw1, dw3, dw2) in ref["dw_routed"].items():
+        werr[f"dw13[{e}]"] = fro_err(got["dw13"][e], _interleave13(dw1, dw3, cfg.inter, cfg.d))
+        werr[f"dw2[{e}]"] = fro_err(got["dw2"][e], dw2)
+    for s, (dw1, dw3, dw2) in enumerate(ref["dw_shared"]):
+        werr[f"dws13[{s}]"] = fro_err(got["dws13"][s], _interleave13(dw1, dw3, cfg.inter, cfg.d))
+        werr[f"dws2[{s}]"] = fro_err(got["dws2"][s], dw2)
+    return errs, werr
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "mid", "tiny_fp8", "ragged_fp8", "ragged_ue8m0", "mid_fp8"])
 def test_backward_matches_oracle(name):
-    cfg = synth.get_config(name)
+    cfg = synth.get_config("mid", prec="fp8") if name == "mid_fp8" else synth.get_config(name)
+    fp8 = cfg.oracle_fp8
     host = HostLayer(cfg)
     layer = host.device_layer()
     u = synth.tokens(cfg)
@@ -54,39 +88,35 @@ def test_backward_matches_oracle(name):
     cnt = torch.empty(cfg.E, dtype=torch.int32, device=DEV)
     capi.moe_route(layer.dims, u.to(DEV), layer.centroids, host.bias.to(DEV), idx, gate, cnt, layer.ws)
     idx = idx.cpu().numpy()
-    ref = ob.layer_backward(synth.bf16_bits(u), synth.bf16_bits(host.cent), idx,
-                            oracle.bf16_to_f64(synth.bf16_bits(dout)), host.routed_bits, host.shared_bits,
-                            cfg.n_shared, cfg.E)
     got = {k: v.cpu().numpy().astype(np.float64) for k, v in g.items()}
-    errs = {"du": rel_err(got["du"], ref["du"]), "dcentroids": rel_err(got["dcentroids"], ref["dcent"])}
-    print(f"{name}: du {errs['du']:.3e}, dcentroids {errs['dcentroids']:.3e} (max|err|/rms)")
-    assert all(v <= BWD_TOL for v in errs.values()), errs
-    I = cfg.inter
-    werr = {}
-    for e, (dw1, dw3, dw2) in ref["dw_routed"].items():
-        # w13 interleave: rows [256j, 256j+128) of W1 block j, [256j+128, 256j+256) of W3 block j
-        ref13 = np.stack([dw1.reshape(I // 128, 128, cfg.d), dw3.reshape(I // 128, 128, cfg.d)], 1).reshape(2 * I, cfg.d)
-        werr[f"dw13[{e}]"] = fro_err(got["dw13"][e], ref13)
-        werr[f"dw2[{e}]"] = fro_err(got["dw2"][e], dw2)
+    oracle_of = lambda act_bf16: ob.layer_backward(
+        synth.bf16_bits(u), synth.bf16_bits(host.cent), idx, oracle.bf16_to_f64(synth.bf16_bits(dout)),
+        host.routed_bits, host.shared_bits, cfg.n_shared, cfg.E, fp8=fp8, act_bf16=act_bf16)
+    for act_bf16 in (True, False):
+        ref = oracle_of(act_bf16)
+        errs, werr = _errors(got, ref, cfg)
+        data_tol, wg_tol = (KP_TOL, KP_WG_TOL) if act_bf16 else EXACT_TOL[bool(fp8)]
+        worst = max(werr, key=werr.get)
+        print(f"{name} vs {'kernel precision' if act_bf16 else 'exact'}: du {errs['du']:.3e}, "
+              f"dcentroids {errs['dcentroids']:.3e} (max|err|/rms); weights worst {worst} {werr[worst]:.3e}")
+        assert all(v <= data_tol for v in errs.values()), errs
+        assert all(v <= wg_tol for v in werr.values()), {k: v for k, v in werr.items() if v > wg_tol}
     for e in set(range(cfg.E)) - set(ref["dw_routed"]):
         assert not got["dw13"][e].any() and not got["dw2"][e].any()
-    for s, (dw1, dw3, dw2) in enumerate(ref["dw_shared"]):
-        ref13 = np.stack([dw1.reshape(I // 128, 128, cfg.d), dw3.reshape(I // 128, 128, cfg.d)], 1).reshape(2 * I, cfg.d)
-        werr[f"dws13[{s}]"] = fro_err(got["dws13"][s], ref13)
-        werr[f"dws2[{s}]"] = fro_err(got["dws2"][s], dw2)
-    worst = max(werr, key=werr.get)
-    print(f"{name}: weight gradients, worst {worst} {werr[worst]:.3e} (relative Frobenius)")
-    assert all(v <= WG_TOL for v in werr.values()), {k: v for k, v in werr.items() if v > WG_TOL}
     # the weight-gradient GEMM's arithmetic: dW2 = dy^T h on the bf16-rounded operands
     x = oracle.bf16_to_f64(synth.bf16_bits(u))
     G = oracle.bf16_to_f64(synth.bf16_bits(dout))
     gate = gate.cpu().numpy().astype(np.float64)
+    pow2 = fp8 == "ue8m0"
     for e in sorted(ref["dw_routed"])[:4]:
-        w1, w3, _ = (oracle.bf16_to_f64(w) for w in host.routed_bits(e))
+        w1, w3, _ = oracle.expert_operands(*host.routed_bits(e), fp8)
         rows, js = np.nonzero(idx == e)
-        a, b = _bf16(x[rows] @ w1.T), _bf16(x[rows] @ w3.T)
+        xr = oracle.fp8_roundtrip_1x128(x[rows], pow2) if fp8 else x[rows]
+        a, b = _bf16(xr @ w1.T), _bf16(xr @ w3.T)
         h = _bf16(a / (1.0 + np.exp(-a)) * b)
         dy = _bf16(gate[rows, js][:, None] * G[rows])
+        if fp8:  # quantised along the tokens, each dequantised value rounded to bf16
+            dy, h = _bf16(ob._q_tok(dy, pow2)), _bf16(ob._q_tok(h, pow2))
         assert fro_err(got["dw2"][e], dy.T @ h) <= REPLAY_TOL, e
 
 
@@ -98,3 +128,32 @@ def test_transpose_expert_weights():
     w2t = torch.empty((E, I, d), dtype=torch.bfloat16, device=DEV)
     capi.moe_transpose_expert_weights(E, I, d, w13, w2, w13t, w2t)
     assert torch.equal(w13t, w13.transpose(1, 2)) and torch.equal(w2t, w2.transpose(1, 2))
+
+
+def test_transpose_expert_weights_fp8():
+    """FP8 codes and block-scale grids transposed per expert equal the
+    quantisation of the transposed bf16 weights (a 128 x 128 block keeps its
+    codes and its scale when transposed)."""
+    E, I, d = 3, 256, 384
+    w13 = torch.randn((E, 2 * I, d), device=DEV).to(torch.bfloat16)
+    w2 = torch.randn((E, d, I), device=DEV).to(torch.bfloat16)
+
+    def quant(w):
+        r, c = w.shape
+        q = torch.empty((r, c), dtype=torch.uint8, device=DEV)
+        s = torch.empty((r // 128, c // 128), dtype=torch.float32, device=DEV)
+        capi.moe_quantize_fp8_blocks(w.contiguous(), r, c, q, s)
+        return q, s
+
+    w13q, w13s = (torch.stack(t) for t in zip(*[quant(w13[e]) for e in range(E)]))
+    w2q, w2s = (torch.stack(t) for t in zip(*[quant(w2[e]) for e in range(E)]))
+    w13t = torch.empty((E, d, 2 * I), dtype=torch.uint8, device=DEV)
+    w2t = torch.empty((E, I, d), dtype=torch.uint8, device=DEV)
+    w13ts = torch.empty((E, d // 128, 2 * I // 128), device=DEV)
+    w2ts = torch.empty((E, I // 128, d // 128), device=DEV)
+    capi.moe_transpose_expert_weights_fp8(E, I, d, w13q, w13s, w2q, w2s, w13t, w13ts, w2t, w2ts)
+    assert torch.equal(w13t, w13q.transpose(1, 2)) and torch.equal(w2t, w2q.transpose(1, 2))
+    assert torch.equal(w13ts, w13s.transpose(1, 2)) and torch.equal(w2ts, w2s.transpose(1, 2))
+    for e in range(E):  # the same as quantising the transposed bf16 weights
+        tq, ts = quant(w13[e].t())
+        assert torch.equal(tq, w13t[e]) and torch.equal(ts, w13ts[e])

@@ -547,3 +547,26 @@ def test_ue8m0_layer_equals_dense_statement(name):
     other = oracle.layer_output(synth.bf16_bits(u), np.arange(cfg.T), r["idx"], r["gate"],
                                 lambda e: _bits(routed[e]), lambda s: _bits(shared[s]), cfg.n_shared, cfg.E, fp8=True)
     assert np.abs(other - out).max() > 1e-6 * scale
+
+
+def test_reciprocal_codes_reading():
+    """quant_1x128(recip=True) takes the codes from x * (1/s): with UE8M0
+    scales 1/s is exact and the codes are those of x / s; with amax/448 scales
+    they agree except where the two fp32 values straddle an E4M3 rounding
+    boundary, and there by one code step."""
+    rng = np.random.default_rng(17)
+    x = rng.standard_normal((64, 1024)) * np.exp(rng.standard_normal((64, 1)))
+    q_p, s_p = oracle.quant_1x128(x, pow2=True)
+    q_pr, s_pr = oracle.quant_1x128(x, pow2=True, recip=True)
+    assert np.array_equal(q_p, q_pr) and np.array_equal(s_p, s_pr)
+    q, s = oracle.quant_1x128(x)
+    q_r, s_r = oracle.quant_1x128(x, recip=True)
+    assert np.array_equal(s, s_r)
+    diff = q != q_r
+    assert diff.mean() < 1e-3
+    v, v_r = oracle.e4m3_decode(q[diff]), oracle.e4m3_decode(q_r[diff])
+    # adjacent codes of the same sign: their magnitudes differ by one step
+    assert np.all(np.sign(v) == np.sign(v_r))
+    assert np.all(np.abs(q[diff].astype(int) - q_r[diff].astype(int)) == 1)
+    # and brute's statement of the same reading agrees with the oracle's codes
+    np.testing.assert_array_equal(brute.quant_dequant(x, 1, 128, recip=True), oracle.dequant_1x128(q_r, s_r))
