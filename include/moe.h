@@ -315,7 +315,9 @@ moe_status moe_forward_replicated(const moe_dims* dims, const moe_weights* w, co
  *
  * moe_backward recomputes the forward's routing, dispatch and expert
  * activations (the same kernels), then:
- *   dy = g G (routed rows), dg = G . y, ds = (dg - sum g dg) / S,
+ *   dy = g G (routed rows), dg = G . y (bf16 layers: as (dh . h) / g, the
+ *   same in exact arithmetic since dh = g G W2, so y is not recomputed),
+ *   ds = (dg - sum g dg) / S,
  *   dz = ds s (1 - s);  dh = dy W2;  da, db from the SwiGLU derivative;
  *   dx = [da db] W13;  du = G + sum_j dx_j + sum_s dx_s + sum_j dz_j c_{e_j};
  *   dW2 = dy^T h, dW13 = [da db]^T x per expert (fp32 GEMMs over the expert's

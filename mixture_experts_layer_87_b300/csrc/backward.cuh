@@ -319,21 +319,67 @@ __global__ void swiglu_bwd_kernel(const __nv_bfloat16* __restrict__ ab, const __
   }
 }
 
-// Backward of the combine and of the gates, one block (128 threads) per token:
-//   dy[slot(t,j)] = g_{t,j} G_t                       (the routed experts' output gradient, bf16)
-//   dg_j = G_t . y[slot(t,j)]                         (fp32, block reduction)
+// Backward of the gates, the last part for one token (block of 128 threads):
+// with dg_j = dL/dg_{t,j} in s_dg[j][warp] (per-warp partial sums):
 //   ds_j = (dg_j - sum_j' g_j' dg_j') / S, S = sum_j s_j;  dz_j = ds_j s_j (1 - s_j)
-//   du_t = G_t + sum_j dz_j c_{e_j}                  (fp32: the residual and the router's share)
-// s_j is recomputed from the router's logits z (the sum of the K splits, as
-// the top-k kernel takes it).  dz_row[slot] = dz_j feeds the centroid gradient.
-__global__ void __launch_bounds__(128) combine_bwd_kernel(
-    const __nv_bfloat16* __restrict__ G, const __nv_bfloat16* __restrict__ y, const int32_t* __restrict__ slot,
-    const int32_t* __restrict__ idx, const float* __restrict__ gate, const float* __restrict__ z, int splits,
-    int64_t split_stride, const __nv_bfloat16* __restrict__ cent, int T, int d, int k, int E, int64_t rows,
-    __nv_bfloat16* __restrict__ dy, float* __restrict__ dz_row, float* __restrict__ du, int* status) {
-  __shared__ int s_slot[32], s_e[32];
-  __shared__ float s_g[32], s_s[32], s_dg[32][4], s_dz[32];
-  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+//   du_t = G_t + sum_j dz_j c_{e_j}                    (fp32: the residual and the router's share)
+// dz_row[slot] = dz_j feeds the centroid gradient.
+struct GateShared {
+  int slot[32], e[32];
+  float g[32], s[32], dg[32][4], dz[32];
+};
+
+__device__ __forceinline__ void gates_tail(GateShared& sh, int t, int k, int d, const __nv_bfloat16* __restrict__ Gt,
+                                           const __nv_bfloat16* __restrict__ cent, float* __restrict__ dz_row,
+                                           float* __restrict__ du) {
+  const int tid = threadIdx.x;
+  __syncthreads();
+  if (tid < 32) {
+    const bool on = tid < k && sh.slot[tid] >= 0;
+    const float dg = on ? sh.dg[tid][0] + sh.dg[tid][1] + sh.dg[tid][2] + sh.dg[tid][3] : 0.0f;
+    float gdg = on ? sh.g[tid] * dg : 0.0f, S = on ? sh.s[tid] : 0.0f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      gdg += __shfl_xor_sync(0xffffffffu, gdg, off);
+      S += __shfl_xor_sync(0xffffffffu, S, off);
+    }
+    float dz = 0.0f;
+    if (on) {
+      const float s = sh.s[tid];
+      // (S underflows only when every selected logit is below about -87; the
+      // gates then came from the log domain and the affinities' own
+      // gradient, s (1 - s), vanishes with them)
+      dz = S > 0.0f ? (dg - gdg) / S * s * (1.0f - s) : 0.0f;
+      dz_row[sh.slot[tid]] = dz;
+    }
+    if (tid < k) sh.dz[tid] = dz;
+  }
+  __syncthreads();
+  const int d8 = d / 8;
+  for (int c8 = tid; c8 < d8; c8 += blockDim.x) {
+    float acc[8];
+    unpack8(reinterpret_cast<const uint4*>(Gt)[c8], acc);
+    for (int j = 0; j < k; ++j) {
+      if (sh.e[j] < 0) continue;
+      float cv[8];
+      unpack8(reinterpret_cast<const uint4*>(cent + (int64_t)sh.e[j] * d)[c8], cv);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(sh.dz[j], cv[i], acc[i]);
+    }
+    float4* o = reinterpret_cast<float4*>(du + (int64_t)t * d) + 2 * c8;
+    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
+
+// The token's selection: slots, experts, gates and the affinities s_j
+// recomputed from the router's logits z (the sum of the K splits, as the
+// top-k kernel takes it).  A bad slot or expert is recorded and skipped.
+__device__ __forceinline__ void gates_head(GateShared& sh, int t, int k, int E, int64_t rows,
+                                           const int32_t* __restrict__ slot, const int32_t* __restrict__ idx,
+                                           const float* __restrict__ gate, const float* __restrict__ z, int splits,
+                                           int64_t split_stride, int* status) {
+  const int tid = threadIdx.x;
   if (tid < k) {
     int sl = slot[(int64_t)t * k + tid], e = idx[(int64_t)t * k + tid];
     if (sl < 0 || sl >= rows || e < 0 || e >= E) {
@@ -341,25 +387,38 @@ __global__ void __launch_bounds__(128) combine_bwd_kernel(
       sl = -1;
       e = -1;
     }
-    s_slot[tid] = sl;
-    s_e[tid] = e;
-    s_g[tid] = gate[(int64_t)t * k + tid];
+    sh.slot[tid] = sl;
+    sh.e[tid] = e;
+    sh.g[tid] = gate[(int64_t)t * k + tid];
     float zz = 0.0f;
     if (e >= 0) {
       zz = z[(int64_t)t * E + e];
       for (int p = 1; p < splits; ++p) zz += z[p * split_stride + (int64_t)t * E + e];
     }
-    s_s[tid] = 1.0f / (1.0f + expf(-zz));
+    sh.s[tid] = 1.0f / (1.0f + expf(-zz));
   }
   __syncthreads();
-  // 8 columns per thread per step (d % 8 == 0): 16-byte loads and stores
+}
+
+// Backward of the combine and of the gates, one block (128 threads) per token:
+//   dy[slot(t,j)] = g_{t,j} G_t                       (the routed experts' output gradient, bf16)
+//   dg_j = G_t . y[slot(t,j)]                         (fp32, block reduction)
+// then gates_tail.  8 columns per thread per step (d % 8 == 0).
+__global__ void __launch_bounds__(128) combine_bwd_kernel(
+    const __nv_bfloat16* __restrict__ G, const __nv_bfloat16* __restrict__ y, const int32_t* __restrict__ slot,
+    const int32_t* __restrict__ idx, const float* __restrict__ gate, const float* __restrict__ z, int splits,
+    int64_t split_stride, const __nv_bfloat16* __restrict__ cent, int T, int d, int k, int E, int64_t rows,
+    __nv_bfloat16* __restrict__ dy, float* __restrict__ dz_row, float* __restrict__ du, int* status) {
+  __shared__ GateShared sh;
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  gates_head(sh, t, k, E, rows, slot, idx, gate, z, splits, split_stride, status);
   const __nv_bfloat16* Gt = G + (int64_t)t * d;
   const int d8 = d / 8;
   for (int j = 0; j < k; ++j) {
-    const int sl = s_slot[j];
+    const int sl = sh.slot[j];
     float part = 0.0f;
     if (sl >= 0) {
-      const float gj = s_g[j];
+      const float gj = sh.g[j];
       for (int c8 = tid; c8 < d8; c8 += blockDim.x) {
         float gv[8], yv[8], o[8];
         unpack8(reinterpret_cast<const uint4*>(Gt)[c8], gv);
@@ -374,44 +433,67 @@ __global__ void __launch_bounds__(128) combine_bwd_kernel(
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    if (lane == 0) s_dg[j][wid] = part;
+    if (lane == 0) sh.dg[j][wid] = part;
   }
-  __syncthreads();
-  if (tid < 32) {
-    const bool on = tid < k && s_slot[tid] >= 0;
-    const float dg = on ? s_dg[tid][0] + s_dg[tid][1] + s_dg[tid][2] + s_dg[tid][3] : 0.0f;
-    float gdg = on ? s_g[tid] * dg : 0.0f, S = on ? s_s[tid] : 0.0f;
+  gates_tail(sh, t, k, d, Gt, cent, dz_row, du);
+}
+
+// dy[slot(t,j)] = g_{t,j} G_t for every routed row (bf16), block per token.
+__global__ void __launch_bounds__(128) scale_rows_kernel(const __nv_bfloat16* __restrict__ G,
+                                                         const int32_t* __restrict__ slot,
+                                                         const float* __restrict__ gate, int k, int d, int64_t rows,
+                                                         __nv_bfloat16* __restrict__ dy) {
+  const int t = blockIdx.x;
+  const uint4* Gt = reinterpret_cast<const uint4*>(G + (int64_t)t * d);
+  const int d8 = d / 8;
+  for (int j = 0; j < k; ++j) {
+    const int sl = slot[(int64_t)t * k + j];
+    if (sl < 0 || sl >= rows) continue;
+    const float gj = gate[(int64_t)t * k + j];
+    uint4* o = reinterpret_cast<uint4*>(dy + (int64_t)sl * d);
+    for (int c8 = threadIdx.x; c8 < d8; c8 += blockDim.x) {
+      float gv[8];
+      unpack8(Gt[c8], gv);
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      gdg += __shfl_xor_sync(0xffffffffu, gdg, off);
-      S += __shfl_xor_sync(0xffffffffu, S, off);
+      for (int i = 0; i < 8; ++i) gv[i] *= gj;
+      o[c8] = pack8_bf16(gv);
     }
-    float dz = 0.0f;
-    if (on) {
-      const float s = s_s[tid];
-      // (S underflows only when every selected logit is below about -87; the
-      // gates then came from the log domain and the affinities' own
-      // gradient, s (1 - s), vanishes with them)
-      dz = S > 0.0f ? (dg - gdg) / S * s * (1.0f - s) : 0.0f;
-      dz_row[s_slot[tid]] = dz;
-    }
-    if (tid < k) s_dz[tid] = dz;
   }
-  __syncthreads();
-  for (int c8 = tid; c8 < d8; c8 += blockDim.x) {
-    float acc[8];
-    unpack8(reinterpret_cast<const uint4*>(Gt)[c8], acc);
-    for (int j = 0; j < k; ++j) {
-      if (s_e[j] < 0) continue;
-      float cv[8];
-      unpack8(reinterpret_cast<const uint4*>(cent + (int64_t)s_e[j] * d)[c8], cv);
+}
+
+// The gates' backward without the experts' outputs y: since dh = dy W2 and
+// dy = g G, the gradient of the gate is
+//   dg_j = G_t . y_r = G_t . (W2 h_r) = (G_t W2) . h_r = (dh_r . h_r) / g_j
+// (r = slot(t, j)), a dot product of two [I] rows the backward holds anyway
+// (0 for a gate that underflowed to 0); then gates_tail.
+__global__ void __launch_bounds__(128) gate_grad_kernel(
+    const __nv_bfloat16* __restrict__ G, const __nv_bfloat16* __restrict__ dh, const __nv_bfloat16* __restrict__ h,
+    int I, const int32_t* __restrict__ slot, const int32_t* __restrict__ idx, const float* __restrict__ gate,
+    const float* __restrict__ z, int splits, int64_t split_stride, const __nv_bfloat16* __restrict__ cent, int d, int k,
+    int E, int64_t rows, float* __restrict__ dz_row, float* __restrict__ du, int* status) {
+  __shared__ GateShared sh;
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  gates_head(sh, t, k, E, rows, slot, idx, gate, z, splits, split_stride, status);
+  const int i8 = I / 8;
+  for (int j = 0; j < k; ++j) {
+    const int sl = sh.slot[j];
+    float part = 0.0f;
+    if (sl >= 0) {
+      const uint4* a = reinterpret_cast<const uint4*>(dh + (int64_t)sl * I);
+      const uint4* b = reinterpret_cast<const uint4*>(h + (int64_t)sl * I);
+      for (int c8 = tid; c8 < i8; c8 += blockDim.x) {
+        float av[8], bv[8];
+        unpack8(a[c8], av);
+        unpack8(b[c8], bv);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(s_dz[j], cv[i], acc[i]);
+        for (int i = 0; i < 8; ++i) part = fmaf(av[i], bv[i], part);
+      }
     }
-    float4* o = reinterpret_cast<float4*>(du + (int64_t)t * d) + 2 * c8;
-    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+    if (lane == 0) sh.dg[j][wid] = sh.g[j] > 0.0f ? part / sh.g[j] : 0.0f;
   }
+  gates_tail(sh, t, k, d, G + (int64_t)t * d, cent, dz_row, du);
 }
 
 // du_t += sum_j dx[slot(t,j)] + sum_s dx_shared[s T + t]   (fp32 accumulation,

@@ -1253,29 +1253,34 @@ moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_we
   void* ab = at<void>(ws, B.ab);
   void* h = at<void>(ws, L.h);
   void* y = at<void>(ws, L.y);
-  // --- routed experts: a, b (gate/up pre-activations), h, y
+  // --- routed experts: a, b (gate/up pre-activations), h.  The experts'
+  // outputs y are not recomputed: the gates' gradient G . y is (dh . h) / g
+  // (gate_grad_kernel), from dh below.
   MOE_TRY(xgemm_bf16(w->w13, E * I2, static_cast<int>(I2), static_cast<int>(D), x, R, ab, I2, static_cast<int>(E),
                      groups, mt_total, cgroup, chunks, 0, 0, queue + 0, status, st));
   swiglu_fwd_kernel<<<ew_blocks(R * I / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab), R, static_cast<int>(I),
                                                        static_cast<__nv_bfloat16*>(h));
   MOE_TRY(launched());
-  MOE_TRY(xgemm_bf16(w->w2, E * D, static_cast<int>(D), static_cast<int>(I), h, R, y, D, static_cast<int>(E), groups,
-                     mt_total, cgroup, chunks, 0, 0, queue + 1, status, st));
-  // --- combine and gates backward: dy, dz, du = G + router share
+  // --- the routed rows' output gradient dy = g G, then dh = dy W2
   void* dy = at<void>(ws, B.dy);
   float* dz_row = at<float>(ws, B.dz_row);
-  const LogitsSplit sp = logits_split(d);
-  combine_bwd_kernel<<<static_cast<unsigned>(T), 128, 0, st>>>(
-      reinterpret_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(y), slot, idx, gate, z,
-      sp.splits, T * E, reinterpret_cast<const __nv_bfloat16*>(w->centroids), static_cast<int>(T), static_cast<int>(D),
-      d.k, static_cast<int>(E), R, static_cast<__nv_bfloat16*>(dy), dz_row, gr->du, status);
+  scale_rows_kernel<<<static_cast<unsigned>(T), 128, 0, st>>>(reinterpret_cast<const __nv_bfloat16*>(dout), slot, gate,
+                                                              d.k, static_cast<int>(D), R,
+                                                              static_cast<__nv_bfloat16*>(dy));
   MOE_TRY(launched());
-  // --- data gradients of the routed experts
   void* dh = at<void>(ws, B.dh);
   void* dab = at<void>(ws, B.dab);
   void* dx = at<void>(ws, B.dx);
   MOE_TRY(xgemm_bf16(wt->w2t, E * I, static_cast<int>(I), static_cast<int>(D), dy, R, dh, I, static_cast<int>(E), groups,
                      mt_total, cgroup, chunks, 0, 0, queue + 2, status, st));
+  // --- gates backward: dz, du = G + router share
+  const LogitsSplit sp = logits_split(d);
+  gate_grad_kernel<<<static_cast<unsigned>(T), 128, 0, st>>>(
+      reinterpret_cast<const __nv_bfloat16*>(dout), static_cast<const __nv_bfloat16*>(dh),
+      static_cast<const __nv_bfloat16*>(h), static_cast<int>(I), slot, idx, gate, z, sp.splits, T * E,
+      reinterpret_cast<const __nv_bfloat16*>(w->centroids), static_cast<int>(D), d.k, static_cast<int>(E), R, dz_row,
+      gr->du, status);
+  MOE_TRY(launched());
   swiglu_bwd_kernel<<<ew_blocks(R * I / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab),
                                                        static_cast<const __nv_bfloat16*>(dh), R, static_cast<int>(I),
                                                        static_cast<__nv_bfloat16*>(dab));

@@ -13,7 +13,14 @@ Two oracle references per case:
    bf16 dx rows whose elements reach a few times rms(du), so a moved rounding
    there is up to ~1.5e-2 of rms(du): data gradients max|err| / rms(ref) <=
    2e-2; weight gradients (fp32 sums of many such values, compared in norm)
-   relative Frobenius norm <= 5e-3.
+   relative Frobenius norm <= 5e-3.  One exception, bf16 only: the kernels
+   take the gates' gradient G . y as (dh . h) / g (equal in exact arithmetic,
+   dh = g G W2), so it carries the bf16 roundings of dy, dh and h (three
+   2^-9 steps) where the oracle's carries y's (one).  That ~2e-3 relative
+   error of dg passes through the gates' Jacobian into dz, and dcentroids sums
+   dz u over an expert's tokens, which point in similar directions (clustered
+   tokens) while dz changes sign, so the sum cancels and its relative error
+   grows several-fold: dcentroids <= 4e-2 there.
 2. The exact arithmetic (fp64 intermediates).  bf16: every intermediate
    rounded to 8 significant bits (2^-9 relative), a gradient through up to
    four such roundings: data gradients max|err| / rms <= 5e-2 (a few roundings
@@ -42,6 +49,7 @@ from parity import HostLayer, rel_err
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 KP_TOL = 2e-2       # against the kernels' precision: data gradients, max|err| / rms(ref)
+KP_DCENT_BF16 = 4e-2  # ... dcentroids of the bf16 path (the gates' gradient from dh . h, see above)
 KP_WG_TOL = 5e-3    # against the kernels' precision: weight gradients, relative Frobenius norm
 EXACT_TOL = {False: (5e-2, 2e-2), True: (1.5e-1, 5e-2)}   # against fp64 intermediates, bf16 / FP8
 REPLAY_TOL = 1e-3   # dW2 against the bf16-operand replay, relative Frobenius norm
@@ -96,10 +104,11 @@ def test_backward_matches_oracle(name):
         ref = oracle_of(act_bf16)
         errs, werr = _errors(got, ref, cfg)
         data_tol, wg_tol = (KP_TOL, KP_WG_TOL) if act_bf16 else EXACT_TOL[bool(fp8)]
+        dcent_tol = KP_DCENT_BF16 if act_bf16 and not fp8 else data_tol
         worst = max(werr, key=werr.get)
         print(f"{name} vs {'kernel precision' if act_bf16 else 'exact'}: du {errs['du']:.3e}, "
               f"dcentroids {errs['dcentroids']:.3e} (max|err|/rms); weights worst {worst} {werr[worst]:.3e}")
-        assert all(v <= data_tol for v in errs.values()), errs
+        assert errs["du"] <= data_tol and errs["dcentroids"] <= dcent_tol, errs
         assert all(v <= wg_tol for v in werr.values()), {k: v for k, v in werr.items() if v > wg_tol}
     for e in set(range(cfg.E)) - set(ref["dw_routed"]):
         assert not got["dw13"][e].any() and not got["dw2"][e].any()
