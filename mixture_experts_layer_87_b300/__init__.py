@@ -14,9 +14,9 @@ from .capi import (MoEError, moe_bias_update, moe_combine, moe_forward, moe_forw
                    moe_pack_gate_up, moe_permute, moe_plan_replicas, moe_quantize_fp8_blocks,
                    moe_read_device_status, moe_route, moe_route_noalloc, moe_selftest_wait_timeout,
                    moe_workspace_size)
-from .layer import HostPipeline, MoELayer, ReplicatedExperts
+from .layer import CapturedForward, HostPipeline, MoELayer, ReplicatedExperts
 
-__all__ = ["capi", "HostPipeline", "MoEError", "MoELayer", "ReplicatedExperts", "moe_forward_replicated",
+__all__ = ["capi", "CapturedForward", "HostPipeline", "MoEError", "MoELayer", "ReplicatedExperts", "moe_forward_replicated",
            "moe_plan_replicas", "moe_bias_update", "moe_combine", "moe_forward", "moe_grouped_ffn",
            "moe_pack_gate_up", "moe_permute", "moe_quantize_fp8_blocks", "moe_read_device_status", "moe_route",
            "moe_route_noalloc", "moe_selftest_wait_timeout", "moe_workspace_size"]

@@ -154,6 +154,37 @@ class MoELayer:
         return capi.moe_read_device_status(self.ws_bwd)
 
 
+class CapturedForward:
+    """The layer's forward recorded once in a CUDA graph and replayed.
+
+    A forward enqueues ~10 kernels and two small memsets and never waits on
+    the device or allocates, so the whole call captures into one graph; a
+    replay then costs one launch from the host.  The graph reads its own
+    input buffer (u is copied in), the bias tensor given here (its current
+    contents at each replay, so moe_bias_update may change it in place) and
+    writes its own output and counts buffers."""
+
+    def __init__(self, layer: MoELayer, bias: torch.Tensor):
+        dev = layer.device
+        self.layer, self.bias = layer, bias
+        self.u = torch.zeros((layer.T, layer.d), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((layer.T, layer.d), dtype=torch.bfloat16, device=dev)
+        self.counts = torch.zeros(layer.E, dtype=torch.int32, device=dev)
+        side = torch.cuda.Stream(device=dev)          # warm-up off the capturing stream, as torch requires
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            layer.forward(self.u, bias, self.out, counts=self.counts)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            layer.forward(self.u, bias, self.out, counts=self.counts)
+
+    def __call__(self, u: torch.Tensor) -> torch.Tensor:
+        self.u.copy_(u)
+        self.graph.replay()
+        return self.out
+
+
 class HostPipeline:
     """The layer over batches that live in pinned host memory.
 
