@@ -57,6 +57,7 @@ def _load():
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
         lib.oracle_quant_1x128.argtypes = [i64, i32, vp, vp, vp, i32, i32]
         lib.oracle_quant_128x128.argtypes = [i64, i32, vp, vp, vp, i32]
+        lib.oracle_dequant.argtypes = [i64, i32, vp, vp, i32, vp]
         lib.oracle_swiglu.argtypes = [i64, i32, i32, vp, vp, vp, vp, i32, vp]
         lib.oracle_bias_update.argtypes = [i32, i64, i32, vp, f32, vp]
         _lib = lib
@@ -185,12 +186,22 @@ def quant_128x128(w: np.ndarray, pow2: bool = False):
     return q, s
 
 
+def _dequant(q: np.ndarray, s: np.ndarray, block_rows: int) -> np.ndarray:
+    q, s = _c(q, np.uint8), _c(s, np.float32)
+    rows, cols = q.shape
+    out = np.empty((rows, cols), np.float64)
+    _load().oracle_dequant(rows, cols, q.ctypes.data, s.ctypes.data, block_rows, out.ctypes.data)
+    return out
+
+
 def dequant_1x128(q: np.ndarray, s: np.ndarray) -> np.ndarray:
-    return e4m3_decode(q) * np.repeat(s.astype(np.float64), 128, axis=1)
+    """E4M3 value of every code times its 1 x 128 tile's scale (fp64)."""
+    return _dequant(q, s, 1)
 
 
 def dequant_128x128(q: np.ndarray, s: np.ndarray) -> np.ndarray:
-    return e4m3_decode(q) * np.repeat(np.repeat(s.astype(np.float64), 128, axis=0), 128, axis=1)
+    """E4M3 value of every code times its 128 x 128 block's scale (fp64)."""
+    return _dequant(q, s, 128)
 
 
 def fp8_roundtrip_1x128(x: np.ndarray, pow2: bool = False, recip: bool = False) -> np.ndarray:

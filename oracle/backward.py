@@ -125,7 +125,7 @@ def _expert_backward_fp8(x, w1, w3, w2, dy, pow2, rb=_identity):
 
 
 def layer_backward(u_bits, cent_bits, idx, G, routed_weights, shared_weights, n_shared: int, E: int,
-                   fp8=False, act_bf16: bool = False) -> dict:
+                   fp8=False, act_bf16: bool = False, keep_dw=None) -> dict:
     """Gradients of the layer for dL/dh' = G [T, d], the selection idx [T, k]
     held fixed.  routed_weights(e) / shared_weights(s) return bf16 bit patterns
     (W1, W3, W2).  Returns dict(du [T, d], dcent [E, d], dw_routed {e: (dW1,
@@ -133,7 +133,9 @@ def layer_backward(u_bits, cent_bits, idx, G, routed_weights, shared_weights, n_
     shared expert, gate [T, k], dgate [T, k]).  fp8: False, True (amax/448
     scales) or "ue8m0" (power-of-two scales): the FP8 scheme of the module
     docstring, whose forward is that of oracle.layer_output(fp8=...).
-    act_bf16: the kernels' bf16 intermediates (module docstring)."""
+    act_bf16: the kernels' bf16 intermediates (module docstring).  keep_dw:
+    the routed experts whose weight gradients dw_routed keeps (None: all; a
+    V3-sized expert's three fp64 gradients take 350 MB)."""
     x = bf16_to_f64(u_bits)
     cent = bf16_to_f64(cent_bits)
     G = np.asarray(G, np.float64)
@@ -168,7 +170,8 @@ def layer_backward(u_bits, cent_bits, idx, G, routed_weights, shared_weights, n_
         dx, dw1, dw3, dw2, y = expert(x[rows], routed_weights(e), dy)
         np.add.at(du, rows, dx)
         dgate[rows, js] = (G[rows] * y).sum(1)
-        dw_routed[e] = (dw1, dw3, dw2)
+        if keep_dw is None or e in keep_dw:
+            dw_routed[e] = (dw1, dw3, dw2)
     # g_j = s_j / S:  ds_j = (dg_j - sum_j' g_j' dg_j') / S;  s = sigmoid(z): dz = ds s (1 - s)
     ds = (dgate - (gate * dgate).sum(1, keepdims=True)) / S
     dz = ds * s_sel * (1.0 - s_sel)

@@ -237,6 +237,19 @@ void oracle_quant_128x128(int64_t rows, int cols, const double* w, uint8_t* q, f
     }
 }
 
+/*
+ * Dequantisation (code value times its scale), fp64: 1 x 128 tiles of a
+ * [rows, cols] matrix (scale [rows, cols/128]) or 128 x 128 blocks (scale
+ * [rows/128, cols/128]).
+ */
+void oracle_dequant(int64_t rows, int cols, const uint8_t* q, const float* scale, int block_rows, double* out) {
+  const int G = cols / 128;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r)
+    for (int c = 0; c < cols; ++c)
+      out[r * cols + c] = oracle_e4m3_decode(q[r * cols + c]) * (double)scale[(r / block_rows) * G + c / 128];
+}
+
 /* ---------------------------------------------------------------------------
  * One SwiGLU expert (ai.flicky.cc practice exercise: three d x d_expert
  * matrices), on n rows:  y = W2 (SiLU(W1 x) * (W3 x)),  SiLU(a) = a sigmoid(a).
