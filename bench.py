@@ -613,7 +613,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="v3", choices=["v3", "v3_fp8", "v3_ue8m0", "v3_nodes", "mid", "decode",
                                                             "v3_slice", "v3_slice_fp8", "decode_slice", "v3_tokens",
-                                                            "v3_tokens_fp8"])
+                                                            "v3_tokens_fp8", "bwd_slice"])
     ap.add_argument("--no-variants", action="store_true", help="skip the mid, FP8 and decode measurements")
     ap.add_argument("--prec", default=None, choices=["bf16", "fp8", "fp8_ue8m0"],
                     help="override the workload's precision")
@@ -621,6 +621,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--ref-tokens", type=int, default=0,
                     help="tokens per step of the reference arm (0: sized so the run takes a few minutes)")
+    ap.add_argument("--backward", action="store_true", help="with --profile-case: backward passes")
     ap.add_argument("--profile-case", action="store_true",
                     help="only build the layer and run warmup+steps forwards (the command ncu wraps)")
     ap.add_argument("--write-traffic", nargs=3, metavar=("KEY", "BYTES", "SOURCE"),
@@ -739,19 +740,30 @@ def profile_case(args):
     """The program ncu wraps: build the workload's layer, run warmup + steps
     forwards (launch order per forward: router GEMM, top-k, scan, plan,
     gather, routed gate/up GEMM, routed down GEMM, shared gate/up GEMM, shared
-    down GEMM, combine), check the device status, exit."""
+    down GEMM, combine) -- or, with --backward, backward passes (after the
+    untimed weight transposes) --, check the device status, exit."""
     torch.cuda.set_device(0)
     cfg = synth.get_config(args.workload, **({"prec": args.prec} if args.prec else {}))
     layer = build_layer(cfg)
     u = synth.tokens(cfg).cuda()
     bias = synth.bias(cfg).cuda()
-    out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
-    for _ in range(args.warmup + args.steps):
-        layer.forward(u, bias, out)
-    torch.cuda.synchronize()
-    st = layer.status()
-    print(json.dumps({"profile_case": cfg.name, "prec": cfg.prec, "forwards": args.warmup + args.steps,
-                      "status": st}))
+    if args.backward:
+        layer.prepare_backward()
+        g = torch.Generator(device="cuda").manual_seed(1)
+        dout = torch.randn((cfg.T, cfg.d), device="cuda", generator=g).to(torch.bfloat16)
+        for _ in range(args.warmup + args.steps):
+            grads = layer.backward(u, bias, dout)
+            del grads
+        torch.cuda.synchronize()
+        st = layer.backward_status()
+    else:
+        out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+        for _ in range(args.warmup + args.steps):
+            layer.forward(u, bias, out)
+        torch.cuda.synchronize()
+        st = layer.status()
+    print(json.dumps({"profile_case": cfg.name, "prec": cfg.prec, "passes": args.warmup + args.steps,
+                      "backward": bool(args.backward), "status": st}))
     if st != 0:
         sys.exit(1)
 

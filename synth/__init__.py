@@ -161,6 +161,11 @@ CONFIGS = {
     # of 256 tokens over 256 experts) with 32 experts, for profiling.
     "decode_slice": LayerConfig("decode_slice", T=32, d=7168, E=32, k=8, n_shared=1, inter=2048,
                                 prec="fp8", bias="zero", rho=V3_RHO, alpha=DECODE_ALPHA),
+    # V3 expert shapes, 8 experts each chosen by all 256 tokens (256 rows per
+    # expert, V3's mean): the backward's kernels at V3 shape on a few GB, for
+    # profiling.
+    "bwd_slice": LayerConfig("bwd_slice", T=256, d=7168, E=8, k=8, n_shared=1, inter=2048,
+                             rho=V3_RHO, alpha=V3_ALPHA),
     # V3 with node-limited routing: 256 experts on 8 nodes of 32, a token's 8
     # experts on at most 4 nodes.
     "v3_nodes": LayerConfig("v3_nodes", T=8192, d=7168, E=256, k=8, n_shared=1, inter=2048,
