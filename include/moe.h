@@ -198,7 +198,10 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, const uint
 
 /*
  * Grouped SwiGLU experts: for g < n_groups, rows [offsets[g], offsets[g+1])
- * of x go through expert g: y = W2_g (SiLU(W1_g x) * (W3_g x)).
+ * of x go through expert g: y = W2_g (SiLU(W1_g x) * (W3_g x)) -- an expert
+ * is three d x I matrices (ai.flicky.cc practice section "Практика:
+ * перепроверяем числа статьи"), FFN_i of the layer equation (ai.flicky.cc
+ * 2.1.2); FP8: the fine-grained scheme of ai.flicky.cc 3.3 items 2-3.
  *   rows      rows allocated in x and y (offsets[n_groups] <= rows).
  *   offsets   [n_groups+1] int32 device array, non-decreasing, offsets[0] = 0.
  *   x         [rows, d] bf16, or E4M3 codes with x_scale [d/128, rows] fp32.
@@ -250,8 +253,10 @@ moe_status moe_bias_update(int32_t E, int32_t T, int32_t k, const int32_t* count
                            float* bias, void* stream);
 
 /*
- * The whole layer: route, dispatch, routed and shared SwiGLU experts,
- * combine.  bias is read only (moe_bias_update is its only writer).
+ * The whole layer (the layer equation of ai.flicky.cc 2.1.2 and xyznot.com
+ * Method 2; FP8 per ai.flicky.cc 3.3): route, dispatch, routed and shared
+ * SwiGLU experts, combine.  bias is read only (moe_bias_update is its only
+ * writer).
  *   u           [T, d] bf16.
  *   out         out [T, d] bf16 (h').
  *   counts_out  out [E] int32 per-expert loads of this step, or NULL.
@@ -400,7 +405,8 @@ moe_status moe_forward_profiled(const moe_dims* dims, const moe_weights* w, cons
 /*
  * Offline weight preparation (not part of the timed layer).
  * moe_pack_gate_up: w13[e] = interleave of w1[e], w3[e] ([E, I, d] bf16 each)
- *   in 128-row blocks, the layout moe_weights.w13 describes.
+ *   in 128-row blocks, the layout moe_weights.w13 describes (a layout of this
+ *   library: the pages name the three matrices, not their storage).
  * moe_quantize_fp8_blocks: w [rows, cols] bf16 -> q [rows, cols] E4M3 codes and
  *   scale [rows/128, cols/128] fp32 with scale = amax/448 of each 128 x 128 block
  *   (1 for an all-zero block), q = round-to-nearest-even, saturating, of w/scale
