@@ -288,7 +288,9 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
 // gather x_perm[slot] = u[t].  FP8: u is quantised once per 1 x 128 tile
 // (scale = amax/448, codes = RNE-saturated E4M3 of u/scale, ai.flicky.cc 3.3
 // item 2) and the codes are copied to every slot; uq/uq_scale (optional)
-// receive the token's own quantised row for the shared experts.
+// receive the token's own quantised row for the shared experts.  With
+// gridDim.y > 1 the row is split into gridDim.y column ranges (more warps for
+// few tokens); every split recomputes the token's slots, split 0 writes them.
 template <bool FP8>
 __global__ void __launch_bounds__(256) dispatch_kernel(
     const int32_t* __restrict__ idx, int T, int k, int E, const uint32_t* __restrict__ mask,
@@ -307,19 +309,22 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
       const int rank = wprefix[(int64_t)e * W + w] + __popc(mask[(int64_t)e * W + w] & ((1u << b) - 1u));
       my_slot = offsets[e] + rank;
       if (!MOE_IN_RANGE(status, my_slot, rows)) my_slot = -1;
-      slot[(int64_t)t * k + lane] = my_slot;
-      if (my_slot >= 0) perm[my_slot] = t;
-    } else {
+      if (blockIdx.y == 0) {
+        slot[(int64_t)t * k + lane] = my_slot;
+        if (my_slot >= 0) perm[my_slot] = t;
+      }
+    } else if (blockIdx.y == 0) {
       slot[(int64_t)t * k + lane] = -1;
     }
   }
+  const int split = blockIdx.y, n_split = gridDim.y;
   const uint4* src = reinterpret_cast<const uint4*>(u + (int64_t)t * d);
   if constexpr (!FP8) {
     uint4* dst = reinterpret_cast<uint4*>(x_perm);
     const int nc = d / 8;
     // every lane runs every iteration (the shuffles need the whole warp);
     // lanes past the row's last 16-byte chunk only skip the copy
-    for (int c0 = 0; c0 < nc; c0 += 32) {
+    for (int c0 = 32 * split; c0 < nc; c0 += 32 * n_split) {
       const int c = c0 + lane;
       const bool act = c < nc;
       const uint4 v = act ? src[c] : make_uint4(0, 0, 0, 0);
@@ -334,7 +339,7 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
     // 16-byte store per destination row (a warp: 512 contiguous bytes).
     const int groups = d / 128;
     const int ql = lane & 7, qw = lane >> 3;
-    for (int g0 = 0; g0 < groups; g0 += 4) {
+    for (int g0 = 4 * split; g0 < groups; g0 += 4 * n_split) {
       const int g = g0 + qw;
       const bool active = g < groups;
       float f0[8], f1[8];
@@ -377,9 +382,10 @@ __global__ void __launch_bounds__(256) dispatch_kernel(
 // ---------------------------------------------------------------------------
 // Combine (ai.flicky.cc 2.1.2, the h'_t equation):
 //   out_t = u_t + sum_s shared_y[s,t] + sum_j gate[t,j] * y[slot[t,j]]
-// fp32 in this fixed order, one rounding to bf16.  One block per token, 16
-// bytes (8 features) per thread per step.  Slots outside [0, rows) are
-// skipped (and flagged).
+// fp32 in this fixed order, one rounding to bf16.  One block per token (per
+// token and column range when gridDim.y > 1, for few tokens), 16 bytes (8
+// features) per thread per step.  Slots outside [0, rows) are skipped (and
+// flagged).
 __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __restrict__ u,
                                                       const __nv_bfloat16* __restrict__ ysh, int n_shared,
                                                       const __nv_bfloat16* __restrict__ y,
@@ -400,7 +406,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const __nv_bfloat16* __res
   }
   __syncthreads();
   const int nc = d / 8;
-  for (int c = threadIdx.x; c < nc; c += blockDim.x) {
+  for (int c = blockIdx.y * blockDim.x + threadIdx.x; c < nc; c += gridDim.y * blockDim.x) {
     float acc[8];
     unpack8(reinterpret_cast<const uint4*>(u + (int64_t)t * d)[c], acc);
     for (int s = 0; s < n_shared; ++s) {

@@ -48,6 +48,7 @@ LogitsSplit logits_split(const moe_dims& d) {
   const int64_t tiles = ((int64_t(d.T) + 127) / 128) * ((int64_t(d.E) + 127) / 128);
   const int num_kb = (d.d + 63) / 64;
   // at most 8 splits: the top-k kernel reads every split's partial logits
+  // (16 made the decode step's router no faster and its top-k slower)
   int64_t want = tiles > 0 ? 148 / tiles : 1;
   if (want > 8) want = 8;
   const int64_t te = int64_t(d.T) * d.E;
@@ -246,6 +247,14 @@ moe_status enqueue_route(const moe_dims& d, const uint16_t* u, const uint16_t* c
 
 // Expert row counts and offsets from the token-expert mask, the GEMM group
 // table, and the gather of permuted rows (FP8: quantised on the way).
+// Column ranges per token of the gather and the combine: one for large
+// batches, more when few tokens would leave most SMs idle (a decode step).
+unsigned token_splits(int T, int d) {
+  if (T >= 2048) return 1;
+  const int chunks = (d / 8 + 127) / 128;  // 128 threads x 16 bytes per range
+  return static_cast<unsigned>(chunks < 8 ? (chunks > 0 ? chunks : 1) : 8);
+}
+
 moe_status enqueue_dispatch(const moe_dims& d, const int32_t* idx, const uint16_t* u, const uint32_t* mask,
                             int32_t* wprefix, int32_t* cnt, int32_t* offsets, GroupEntry* groups, int32_t* mt_total,
                             int32_t* cgroup, int32_t* perm, int32_t* slot, void* x, float* xs, uint8_t* uq, float* uqs, int* status,
@@ -259,7 +268,7 @@ moe_status enqueue_dispatch(const moe_dims& d, const int32_t* idx, const uint16_
   MOE_TRY(launched());
   if (rec) MOE_TRY(rec->mark());
   if (d.T == 0) return rec ? rec->mark() : MOE_OK;  // the offsets (all zero) are the whole result
-  const unsigned blocks = static_cast<unsigned>(cdiv(int64_t(d.T) * 32, 256));
+  const dim3 blocks(static_cast<unsigned>(cdiv(int64_t(d.T) * 32, 256)), token_splits(d.T, d.d));
   const int64_t rows = int64_t(d.T) * d.k;
   const __nv_bfloat16* ub = reinterpret_cast<const __nv_bfloat16*>(u);
   if (is_fp8(d))
@@ -597,7 +606,7 @@ moe_status moe_combine(const moe_dims* dims, const uint16_t* u, const uint16_t* 
   if (!aligned16(u) || !aligned16(y_perm) || !aligned16(out) || (shared_y && !aligned16(shared_y)))
     return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  combine_kernel<<<dims->T, 128, 0, st>>>(
+  combine_kernel<<<dim3(static_cast<unsigned>(dims->T), token_splits(dims->T, dims->d)), 128, 0, st>>>(
       reinterpret_cast<const __nv_bfloat16*>(u), reinterpret_cast<const __nv_bfloat16*>(shared_y), dims->n_shared,
       reinterpret_cast<const __nv_bfloat16*>(y_perm), slot, topk_gate, dims->T, dims->d, dims->k,
       int64_t(dims->T) * dims->k, reinterpret_cast<__nv_bfloat16*>(out), nullptr);
@@ -709,7 +718,7 @@ moe_status forward_impl(const moe_dims* dims, const moe_weights* w, const uint16
     MOE_TRY(rec->mark());
   }
 
-  combine_kernel<<<d.T, 128, 0, st>>>(
+  combine_kernel<<<dim3(static_cast<unsigned>(d.T), token_splits(d.T, d.d)), 128, 0, st>>>(
       reinterpret_cast<const __nv_bfloat16*>(u), reinterpret_cast<const __nv_bfloat16*>(ysh), d.n_shared,
       at<const __nv_bfloat16>(ws, L.y), slot, gate, d.T, d.d, d.k, R, reinterpret_cast<__nv_bfloat16*>(out), status);
   MOE_TRY(launched());
