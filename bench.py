@@ -548,6 +548,24 @@ def measure_decode(args, world, pk, layer=None):
                          for m, g, x in zip(step_ms, gbs, c)]}
 
 
+def measure_replicated(layer, cfg, res, args, world, n_extra=32):
+    """moe_forward_replicated on the same batch: n_extra copies of the most
+    loaded experts, planned from this batch's loads (the copies share the
+    weights on one GPU; the output is moe_forward's)."""
+    from mixture_experts_layer_87_b300 import ReplicatedExperts
+    rep = ReplicatedExperts(layer, torch.from_numpy(res["counts"]), n_extra)
+    u = res["u_host"].cuda()
+    out = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device="cuda")
+    ms = time_forward(rep, u, res["bias"], out, args.steps, args.warmup, world)
+    if rep.status() != 0:
+        raise RuntimeError(f"replicated forward device status {rep.status()}")
+    copies = rep.replica_count_host.numpy()
+    per_copy = res["counts"] / copies
+    return {"value": round(world * cfg.T / (ms * 1e-3), 1), "unit": UNIT, "ms_per_step": round(ms, 4),
+            "n_extra": n_extra, "max_over_mean_load_per_copy": round(float(per_copy.max() / per_copy.mean()), 3),
+            "note": "moe_forward_replicated, the extra copies planned from this batch's loads"}
+
+
 def measure_backward(layer, cfg, u, bias, pk, steps=5, warmup=3):
     """The layer's backward pass on the same batch (bf16, or the FP8 scheme for
     an FP8 layer): dL/dh' a seeded Gaussian, all gradients (du, dcentroids,
@@ -677,6 +695,7 @@ def main():
 
     variants = {}
     if not args.no_variants and args.workload == "v3":
+        variants["v3_replicated"] = measure_replicated(layer, cfg, res, args, world)
         variants["v3_backward"] = measure_backward(layer, cfg, res["u_host"].cuda(), res["bias"], pk)
         del layer, res["layer"]
         torch.cuda.empty_cache()
