@@ -344,7 +344,9 @@ moe_status moe_forward_replicated(const moe_dims* dims, const moe_weights* w, co
  *          dw13 [E, 2I, d] and dw2 [E, d, I] in the layout of w13 and w2 (an
  *          expert no token chose gets zeros); dws13, dws2 the same for the
  *          shared experts (unused when n_shared == 0).  du and the weight
- *          gradients must be 16-byte aligned (else MOE_ERR_INVALID_ARG).
+ *          gradients must be 16-byte aligned (else MOE_ERR_INVALID_ARG).  With
+ *          T == 0, u, dout and du may be NULL and the other gradients are
+ *          zeroed.
  *   ws     at least moe_backward_workspace_size bytes.
  */
 typedef struct {

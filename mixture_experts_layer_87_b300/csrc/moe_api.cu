@@ -1213,7 +1213,8 @@ moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_we
   if (!wt || !wt->w13t || !wt->w2t || (d.n_shared > 0 && (!wt->ws13t || !wt->ws2t))) return MOE_ERR_INVALID_ARG;
   if (is_fp8(d) && (!wt->w13t_scale || !wt->w2t_scale || (d.n_shared > 0 && (!wt->ws13t_scale || !wt->ws2t_scale))))
     return MOE_ERR_INVALID_ARG;
-  if (!gr || !gr->du || !gr->dcentroids || !gr->dw13 || !gr->dw2 || (d.n_shared > 0 && (!gr->dws13 || !gr->dws2)))
+  if (!gr || (d.T > 0 && !gr->du) || !gr->dcentroids || !gr->dw13 || !gr->dw2 ||
+      (d.n_shared > 0 && (!gr->dws13 || !gr->dws2)))
     return MOE_ERR_INVALID_ARG;
   // vector stores of du, TMA stores of the weight gradients
   if (!aligned16(gr->du) || !aligned16(gr->dw13) || !aligned16(gr->dw2) ||

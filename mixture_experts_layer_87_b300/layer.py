@@ -130,19 +130,26 @@ class MoELayer:
                 capi.moe_transpose_expert_weights(self.n_shared, I, d, self.ws13, self.ws2, self.ws13t, self.ws2t)
         self.ws_bwd = torch.empty(capi.moe_backward_workspace_size(self.dims), dtype=torch.uint8, device=dev)
 
-    def backward(self, u: torch.Tensor, bias: torch.Tensor, dout: torch.Tensor, stream=None) -> dict:
-        """Gradients (fp32) of the layer for dL/dh' = dout: du, dcentroids,
-        dw13/dw2 (routed, in the w13/w2 layouts) and dws13/dws2 (shared); for
-        an FP8 layer in the FP8 scheme of moe_backward."""
-        if not hasattr(self, "ws_bwd"):
-            self.prepare_backward()
+    def grad_buffers(self) -> dict:
+        """Uninitialised fp32 gradient tensors in the shapes backward() writes."""
         dev, I, d, f = self.device, self.inter, self.d, torch.float32
         ns = max(self.n_shared, 1)
-        g = dict(du=torch.empty((self.T, d), dtype=f, device=dev), dcentroids=torch.empty((self.E, d), dtype=f, device=dev),
-                 dw13=torch.empty((self.E, 2 * I, d), dtype=f, device=dev),
-                 dw2=torch.empty((self.E, d, I), dtype=f, device=dev),
-                 dws13=torch.empty((ns, 2 * I, d), dtype=f, device=dev),
-                 dws2=torch.empty((ns, d, I), dtype=f, device=dev))
+        return dict(du=torch.empty((self.T, d), dtype=f, device=dev),
+                    dcentroids=torch.empty((self.E, d), dtype=f, device=dev),
+                    dw13=torch.empty((self.E, 2 * I, d), dtype=f, device=dev),
+                    dw2=torch.empty((self.E, d, I), dtype=f, device=dev),
+                    dws13=torch.empty((ns, 2 * I, d), dtype=f, device=dev),
+                    dws2=torch.empty((ns, d, I), dtype=f, device=dev))
+
+    def backward(self, u: torch.Tensor, bias: torch.Tensor, dout: torch.Tensor, stream=None,
+                 grads: dict | None = None) -> dict:
+        """Gradients (fp32) of the layer for dL/dh' = dout: du, dcentroids,
+        dw13/dw2 (routed, in the w13/w2 layouts) and dws13/dws2 (shared); for
+        an FP8 layer in the FP8 scheme of moe_backward.  grads: tensors from
+        grad_buffers() to overwrite (every element is written), else new ones."""
+        if not hasattr(self, "ws_bwd"):
+            self.prepare_backward()
+        g = self.grad_buffers() if grads is None else grads
         ptr = lambda t: t.data_ptr() if t is not None else None
         wt = capi.moe_weights_t(ptr(self.w13t), ptr(self.w2t), ptr(self.ws13t), ptr(self.ws2t), ptr(self.w13t_scale),
                                 ptr(self.w2t_scale), ptr(self.ws13t_scale), ptr(self.ws2t_scale))

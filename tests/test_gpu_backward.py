@@ -31,6 +31,13 @@ Two oracle references per case:
    (2^-3 to 2^-4 of the element): a few percent of the codes, in up to three
    quantised operands in series, about 2% rms each in a K-long product:
    data gradients max|err| / rms <= 1.5e-1, weight gradients Frobenius <= 5e-2.
+   bf16 dcentroids carry both error sources, the (dh . h) / g form of the
+   gates' gradient (4e-2, above) and the bf16 roundings of the intermediates
+   (5e-2), so their exact bound is the sum, 9e-2.  With few tokens the second
+   one alone reaches the 5e-2: an expert's row sums dz u over one or two
+   tokens, so the cancellation in dz is not averaged out (the oracle in the
+   kernels' precision is 2.2e-2 / 4.7e-2 / 3.1e-2 from the exact one at 1 / 2 /
+   4 tokens of the tiny shape, 1.5e-2 at 64).
 
 And the weight-gradient arithmetic itself: dW2 of the first experts against
 the same product replayed from bf16-rounded a, b, h and dy (fp64; FP8: the
@@ -52,6 +59,7 @@ KP_TOL = 2e-2       # against the kernels' precision: data gradients, max|err| /
 KP_DCENT_BF16 = 4e-2  # ... dcentroids of the bf16 path (the gates' gradient from dh . h, see above)
 KP_WG_TOL = 5e-3    # against the kernels' precision: weight gradients, relative Frobenius norm
 EXACT_TOL = {False: (5e-2, 2e-2), True: (1.5e-1, 5e-2)}   # against fp64 intermediates, bf16 / FP8
+EXACT_DCENT_BF16 = KP_DCENT_BF16 + EXACT_TOL[False][0]   # ... dcentroids of the bf16 path: both sources add
 REPLAY_TOL = 1e-3   # dW2 against the bf16-operand replay, relative Frobenius norm
 
 
@@ -69,7 +77,11 @@ def _interleave13(dw1, dw3, I, d):
 
 
 def _errors(got, ref, cfg):
-    errs = {"du": rel_err(got["du"], ref["du"]), "dcentroids": rel_err(got["dcentroids"], ref["dcent"])}
+    errs = {"du": rel_err(got["du"], ref["du"])}
+    if np.any(ref["dcent"]):
+        errs["dcentroids"] = rel_err(got["dcentroids"], ref["dcent"])
+    else:  # k = 1: every gate is s / s = 1, a constant, so the centroids get no gradient
+        errs["dcentroids"] = float(np.abs(got["dcentroids"]).max() / np.sqrt((ref["du"] ** 2).mean()))
     werr = {}
     for e, (dw1, dw3, dw2) in ref["dw_routed"].items():
         werr[f"dw13[{e}]"] = fro_err(got["dw13"][e], _interleave13(dw1, dw3, cfg.inter, cfg.d))
@@ -80,15 +92,23 @@ def _errors(got, ref, cfg):
     return errs, werr
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "mid", "tiny_fp8", "ragged_fp8", "ragged_ue8m0", "mid_fp8"])
-def test_backward_matches_oracle(name):
-    cfg = synth.get_config("mid", prec="fp8") if name == "mid_fp8" else synth.get_config(name)
+def backward_parity(cfg, host_bias=None, exact_dcent=True):
+    """One moe_backward of cfg's seeded layer against the oracle in the
+    kernels' precision and in exact arithmetic (the bounds above;
+    exact_dcent=False leaves dcentroids out of the exact comparison); experts
+    that no token chose must get exactly zero weight gradients (the outputs
+    start as NaN, so every checked element has been written).  host_bias
+    replaces the seeded routing bias.  Returns the GPU's gradients, the
+    selection and the kernel-precision reference."""
     fp8 = cfg.oracle_fp8
     host = HostLayer(cfg)
+    if host_bias is not None:
+        host.bias = host_bias
     layer = host.device_layer()
     u = synth.tokens(cfg)
     dout = synth.normal_bf16(synth.key(cfg.seed, "tokens", 999), (cfg.T, cfg.d), 1.0)
-    g = layer.backward(u.to(DEV), host.bias.to(DEV), dout.to(DEV))
+    g = {k: torch.full_like(v, float("nan")) for k, v in layer.grad_buffers().items()}  # all must be written
+    layer.backward(u.to(DEV), host.bias.to(DEV), dout.to(DEV), grads=g)
     assert layer.backward_status() == 0
     # the selection the backward recomputed
     idx = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=DEV)
@@ -100,22 +120,31 @@ def test_backward_matches_oracle(name):
     oracle_of = lambda act_bf16: ob.layer_backward(
         synth.bf16_bits(u), synth.bf16_bits(host.cent), idx, oracle.bf16_to_f64(synth.bf16_bits(dout)),
         host.routed_bits, host.shared_bits, cfg.n_shared, cfg.E, fp8=fp8, act_bf16=act_bf16)
+    refs = {}
     for act_bf16 in (True, False):
-        ref = oracle_of(act_bf16)
+        ref = refs[act_bf16] = oracle_of(act_bf16)
         errs, werr = _errors(got, ref, cfg)
         data_tol, wg_tol = (KP_TOL, KP_WG_TOL) if act_bf16 else EXACT_TOL[bool(fp8)]
-        dcent_tol = KP_DCENT_BF16 if act_bf16 and not fp8 else data_tol
+        dcent_tol = data_tol if fp8 else (KP_DCENT_BF16 if act_bf16 else EXACT_DCENT_BF16)
         worst = max(werr, key=werr.get)
-        print(f"{name} vs {'kernel precision' if act_bf16 else 'exact'}: du {errs['du']:.3e}, "
+        print(f"{cfg.name} vs {'kernel precision' if act_bf16 else 'exact'}: du {errs['du']:.3e}, "
               f"dcentroids {errs['dcentroids']:.3e} (max|err|/rms); weights worst {worst} {werr[worst]:.3e}")
-        assert errs["du"] <= data_tol and errs["dcentroids"] <= dcent_tol, errs
+        assert errs["du"] <= data_tol, errs
+        assert errs["dcentroids"] <= dcent_tol or (not act_bf16 and not exact_dcent), errs
         assert all(v <= wg_tol for v in werr.values()), {k: v for k, v in werr.items() if v > wg_tol}
-    for e in set(range(cfg.E)) - set(ref["dw_routed"]):
+    for e in set(range(cfg.E)) - set(refs[True]["dw_routed"]):
         assert not got["dw13"][e].any() and not got["dw2"][e].any()
+    return got, idx, gate.cpu().numpy().astype(np.float64), host, u, dout, refs[True]
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "mid", "tiny_fp8", "ragged_fp8", "ragged_ue8m0", "mid_fp8"])
+def test_backward_matches_oracle(name):
+    cfg = synth.get_config("mid", prec="fp8") if name == "mid_fp8" else synth.get_config(name)
+    fp8 = cfg.oracle_fp8
+    got, idx, gate, host, u, dout, ref = backward_parity(cfg)
     # the weight-gradient GEMM's arithmetic: dW2 = dy^T h on the bf16-rounded operands
     x = oracle.bf16_to_f64(synth.bf16_bits(u))
     G = oracle.bf16_to_f64(synth.bf16_bits(dout))
-    gate = gate.cpu().numpy().astype(np.float64)
     pow2 = fp8 == "ue8m0"
     for e in sorted(ref["dw_routed"])[:4]:
         w1, w3, _ = oracle.expert_operands(*host.routed_bits(e), fp8)

@@ -9,6 +9,11 @@ against the CPU oracle:
     runs the widest top-k variant (32 experts per lane);
   * every token routed to the same k experts (a fully skewed load: the other
     experts are empty groups).
+The backward pass (moe_backward) is held to the same edges: an empty batch
+(every gradient zero), one token, the one-expert top-1 layer (a dense SwiGLU,
+whose centroids get no gradient since the one gate is s / s = 1), no shared
+expert, and the fully skewed load (the empty experts' weight gradients exactly
+zero), each against the backward oracle with the bounds of the backward tests.
 """
 from dataclasses import replace
 
@@ -19,6 +24,7 @@ import torch
 import synth
 from mixture_experts_layer_87_b300 import MoELayer, capi
 from parity import TOL, Y_TOL
+from test_gpu_backward import backward_parity
 from test_gpu_parity import _forward_parity
 
 pytestmark = pytest.mark.gpu
@@ -137,3 +143,51 @@ def test_gates_when_every_selected_affinity_underflows():
     assert np.isfinite(gate).all()
     np.testing.assert_allclose(gate.sum(1), 1.0, atol=1e-6)
     np.testing.assert_allclose(gate, oracle.gates_for(r["s_all"], idx), rtol=0, atol=2e-6)
+
+
+@pytest.mark.parametrize("prec", ["bf16", "fp8"])
+def test_backward_empty_batch(prec):
+    cfg = synth.get_config("tiny")
+    layer = MoELayer(0, 256, 16, 4, 1, 128, prec)
+    for e in range(16):
+        layer.load_expert(e, *synth.expert_weights(cfg, e))
+    layer.load_expert(0, *synth.expert_weights(cfg, 0, shared=True), shared=True)
+    layer.set_centroids(synth.centroids(cfg))
+    u = torch.empty((0, 256), dtype=torch.bfloat16, device=DEV)
+    g = {k: torch.full_like(v, float("nan")) for k, v in layer.grad_buffers().items()}
+    layer.backward(u, torch.zeros(16, device=DEV), u, grads=g)
+    torch.cuda.synchronize()
+    assert layer.backward_status() == 0
+    assert g["du"].shape == (0, 256)
+    for k in ("dcentroids", "dw13", "dw2", "dws13", "dws2"):
+        assert not g[k].any(), k
+
+
+@pytest.mark.parametrize("name", ["tiny", "tiny_fp8"])
+def test_backward_single_token(name):
+    # dcentroids only against the oracle in the kernels' precision: with one
+    # token an expert's row is dz u, and dz = (dg_j - sum_i g_i dg_i) terms can
+    # cancel, so the bf16 / E4M3 roundings of the intermediates move it by an
+    # unbounded relative amount (the two oracle modes alone are 2.2e-2 apart in
+    # bf16 and 6.2e-1 in FP8 at this token, 1.5e-2 and 9.2e-2 at 64 tokens).
+    backward_parity(_cfg(name, T=1), exact_dcent=False)
+
+
+@pytest.mark.parametrize("prec", ["bf16", "fp8"])
+def test_backward_one_expert_top1_no_shared(prec):
+    got, *_ = backward_parity(_cfg("tiny", E=1, k=1, n_shared=0, prec=prec))
+    assert not got["dcentroids"].any()
+
+
+@pytest.mark.parametrize("name", ["ragged", "ragged_fp8"])
+def test_backward_no_shared_expert(name):
+    backward_parity(_cfg(name, n_shared=0))
+
+
+@pytest.mark.parametrize("prec", ["bf16", "fp8"])
+def test_backward_all_tokens_on_the_same_experts(prec):
+    cfg = _cfg("tiny", prec=prec, bias="zero")
+    host_bias = torch.zeros(cfg.E)
+    host_bias[[3, 5, 11, 12]] = 10.0
+    got, idx, *_ = backward_parity(cfg, host_bias)
+    assert (np.sort(idx, 1) == [3, 5, 11, 12]).all()
