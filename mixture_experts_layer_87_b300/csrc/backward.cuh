@@ -26,157 +26,204 @@ namespace moe {
 // of group g (offsets[g] .. offsets[g+1]) become columns pad_off[g] .., every
 // group padded to a multiple of `gran` columns (64: one 64-wide K stage of the
 // GEMM; 128 in the FP8 scheme, so that 128-token quantisation blocks start at
-// every group's first token; the padding is zero).  row_of_col[col] = the row a column holds, or -1 for
-// a padding column, for all n_cols columns.  One block: the prefix is serial
-// (G is at most a few thousand), the columns are block-strided.
+// every group's first token; the padding is zero).  row_of_col[col] = the row a
+// column holds, or -1 for a padding column, for the live columns
+// col < pad_off[G] (the columns past it are never read).  One block of 1024
+// threads: the padded sizes are prefix-summed across the block (two groups a
+// thread, G <= 2048), then each thread finds its columns' groups by bisection.
 __global__ void __launch_bounds__(1024) pad_plan_kernel(const int32_t* __restrict__ offsets, int G, int n_cols,
                                                         int gran, int32_t* __restrict__ pad_off,
                                                         int32_t* __restrict__ row_of_col, int* status) {
   __shared__ int s_off[2049];
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int g = 0; g <= G; ++g) {
-      if (g <= 2048) s_off[g] = acc;
-      pad_off[g] = acc;
-      if (g < G) acc += (offsets[g + 1] - offsets[g] + gran - 1) / gran * gran;
-    }
-    if (acc > n_cols) record_status(status, ST_BAD_INDEX);
-  }
-  __syncthreads();
+  __shared__ int s_warp[32];
   if (G > 2048) {  // not used by the library (G <= E + n_shared <= 2048)
     if (threadIdx.x == 0) record_status(status, ST_BAD_INDEX);
     return;
   }
-  for (int col = threadIdx.x; col < n_cols; col += blockDim.x) {
-    int r = -1;
-    if (col < s_off[G]) {
-      int lo = 0, hi = G;  // g with s_off[g] <= col < s_off[g + 1]
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (s_off[mid] <= col) lo = mid;
-        else hi = mid;
-      }
-      const int local = col - s_off[lo];
-      if (local < offsets[lo + 1] - offsets[lo]) r = offsets[lo] + local;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int sz[2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int g = 2 * tid + q;
+    sz[q] = g < G ? (offsets[g + 1] - offsets[g] + gran - 1) / gran * gran : 0;
+  }
+  // inclusive scan of the thread's pair sums: within the warp, then across warps
+  int incl = sz[0] + sz[1];
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
+  }
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = s_warp[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += o;
     }
-    row_of_col[col] = r;
+    s_warp[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int excl = incl - (sz[0] + sz[1]) + (warp > 0 ? s_warp[warp - 1] : 0);
+  if (2 * tid < G) s_off[2 * tid] = excl;
+  if (2 * tid + 1 < G) s_off[2 * tid + 1] = excl + sz[0];
+  if (tid == 0) s_off[G] = s_warp[31];  // the padded total
+  __syncthreads();
+  for (int g = tid; g <= G; g += blockDim.x) pad_off[g] = s_off[g];
+  const int live = s_off[G];
+  if (tid == 0 && live > n_cols) record_status(status, ST_BAD_INDEX);
+  const int end = min(live, n_cols);
+  for (int col = tid; col < end; col += blockDim.x) {
+    int lo = 0, hi = G;  // g with s_off[g] <= col < s_off[g + 1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_off[mid] <= col) lo = mid;
+      else hi = mid;
+    }
+    const int local = col - s_off[lo];
+    row_of_col[col] = local < offsets[lo + 1] - offsets[lo] ? offsets[lo] + local : -1;
   }
 }
 
 // Transposed gather, batched over blockIdx.z (src/dst strides per batch):
-//   dst[c][col] = src[row(col)][c]  for c < C, col < n_cols,
-// row(col) = row_of_col[col] (-1: a zero column) or, with row_of_col ==
-// nullptr, col itself while col < rows (zero beyond).  Every dst column is
-// written, padding included.  64 x 64 tiles through shared memory: 16-byte
-// loads along the src rows, 128 contiguous bytes per warp along the dst rows.
-// Needs C % 8 == 0, 16-byte aligned src rows and an even ldd.
-__global__ void __launch_bounds__(256) transpose_bf16_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C,
-                                                             int64_t src_batch, const int32_t* __restrict__ row_of_col,
-                                                             int n_cols, __nv_bfloat16* __restrict__ dst, int64_t ldd,
-                                                             int64_t dst_batch) {
-  __shared__ uint16_t tile[64][66];  // [c - c0][col - col0]
-  src += blockIdx.z * src_batch;
-  dst += blockIdx.z * dst_batch;
-  const int c0 = blockIdx.x * 64, col0 = blockIdx.y * 64, tid = threadIdx.x;
-  const int chunk = tid & 7;  // 8 columns c of the src row
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int cl = (tid >> 3) + 32 * i, col = col0 + cl;
-    int r = -1;
-    if (col < n_cols) r = row_of_col ? row_of_col[col] : (col < rows ? col : -1);
-    const int c = c0 + chunk * 8;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r >= 0 && r < rows && c < C) v = *reinterpret_cast<const uint4*>(src + (int64_t)r * C + c);
-    const uint16_t* e = reinterpret_cast<const uint16_t*>(&v);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) tile[chunk * 8 + j][cl] = e[j];
-  }
-  __syncthreads();
-  const int p = tid & 31;  // column pair col0 + 2p, + 1
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int cl = (tid >> 5) + 8 * i, c = c0 + cl, col = col0 + 2 * p;
-    if (c >= C || col >= n_cols) continue;
-    const uint32_t pair = *reinterpret_cast<const uint32_t*>(&tile[cl][2 * p]);
-    __nv_bfloat16* o = dst + (int64_t)c * ldd + col;
-    if (col + 1 < n_cols) *reinterpret_cast<uint32_t*>(o) = pair;
-    else *reinterpret_cast<uint16_t*>(o) = static_cast<uint16_t>(pair & 0xFFFF);
-  }
-}
-
-// Transposed gather with the FP8 quantisation of the weight-gradient operands
-// (1 x 128 tiles along the tokens, ai.flicky.cc 3.3 items 2 and 4), written
-// back dequantised as bf16 for the weight-gradient GEMM:
+//   dst[c][col] = f(src[row(col)][c])  for c < C and the live columns col,
+// row(col) = perm[row_of_col[col]] when perm is given, else row_of_col[col]
+// (-1: a zero column), or col itself while col < rows when row_of_col is null
+// (zero beyond).  Live columns: col < n_cols, and col < *n_live when n_live is
+// given (the padded total of the groups: the tiles past it are not written,
+// since nothing reads them, and the columns past it in the last tile are zero).
+//
+// f is the identity (FQ = false), or (FQ = true) the FP8 quantisation of the
+// weight-gradient operands (1 x 128 tiles along the tokens, ai.flicky.cc 3.3
+// items 2 and 4) written back dequantised as bf16:
 //   dst[c][col] = bf16( E4M3(x * (1/s)) * s ),  x = src[row(col)][c],
 // s = amax/448 over the 128-column block of col (UE8M0: rounded up to a power
 // of two; an all-zero block: 1), 1/s one correctly rounded fp32 reciprocal
 // per block (the operands are intermediates known to bf16 accuracy; a
-// division per element would cost more than the copy).  row(col)
-// = perm[row_of_col[col]] when perm is given, else row_of_col[col] (-1: a zero
-// column), or col itself while col < rows when row_of_col is null.  With
-// power-of-two scales the bf16 value is the E4M3 value exactly.  Tiles of
-// 128 columns x 64 c, every dst column written; C % 8 == 0, an even ldd, 16-byte aligned
-// src rows.
-__global__ void __launch_bounds__(256) transpose_fq_kernel(const __nv_bfloat16* __restrict__ src, int rows, int C,
-                                                           int64_t src_batch, const int32_t* __restrict__ row_of_col,
-                                                           const int32_t* __restrict__ perm, int n_cols,
-                                                           __nv_bfloat16* __restrict__ dst, int64_t ldd,
-                                                           int64_t dst_batch, bool pow2) {
-  __shared__ float tile[64][129];  // [c - c0][col - col0]
+// division per element would cost more than the copy).  With power-of-two
+// scales the bf16 value is the E4M3 value exactly.
+//
+// A block owns one 128-column tile (one quantisation block) and walks the c
+// range in 64-wide slabs, blockIdx.x, blockIdx.x + gridDim.x, ...: it looks
+// up its columns' rows once, and loads the next slab (16-byte loads along the
+// src rows, held in registers) while it writes the current one out of shared
+// memory (FQ: four lanes per dst row, 16-byte stores; else a warp per dst row,
+// 4-byte bf16 pairs).  Needs C % 8 == 0, 16-byte aligned src rows, an even ldd
+// and a 4-byte aligned dst; FQ also ldd % 8 == 0 and a 16-byte aligned dst.
+template <bool FQ>
+__global__ void __launch_bounds__(256, 6) transpose_cols_kernel(
+    const __nv_bfloat16* __restrict__ src, int rows, int C, int64_t src_batch, const int32_t* __restrict__ row_of_col,
+    const int32_t* __restrict__ perm, int n_cols, const int32_t* __restrict__ n_live, __nv_bfloat16* __restrict__ dst,
+    int64_t ldd, int64_t dst_batch, bool pow2) {
+  __shared__ __align__(16) uint16_t tile[64][130];  // [c - c0][col - col0]
+  const int col0 = blockIdx.y * 128;
+  const int live = n_live ? min(*n_live, n_cols) : n_cols;
+  if (col0 >= live) return;
   src += blockIdx.z * src_batch;
   dst += blockIdx.z * dst_batch;
-  const int c0 = blockIdx.x * 64, col0 = blockIdx.y * 128, tid = threadIdx.x;
-  const int chunk = tid & 7;  // 8 columns c of the src row
+  const int tid = threadIdx.x, chunk = tid & 7;  // chunk: 8 c values of a src row
+  int row[4];                                     // src rows of my 4 columns, -1: zero column
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int cl = (tid >> 3) + 32 * i, col = col0 + cl;
+    const int col = col0 + (tid >> 3) + 32 * i;
     int r = -1;
-    if (col < n_cols) {
+    if (col < live) {
       r = row_of_col ? row_of_col[col] : (col < rows ? col : -1);
       if (r >= 0 && perm) r = perm[r];
     }
-    const int c = c0 + chunk * 8;
-    float f[8];
-    if (r >= 0 && r < rows && c < C) {
-      unpack8(*reinterpret_cast<const uint4*>(src + (int64_t)r * C + c), f);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) f[j] = 0.0f;
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) tile[chunk * 8 + j][cl] = f[j];
+    row[i] = r >= 0 && r < rows ? r : -1;
   }
-  __syncthreads();
-  // a warp per dst row (8 rows per warp, two at a time): lane l holds the
-  // column pairs 2l and 64 + 2l, written as 4-byte bf16 pairs
+  const int n_slab = (C + 63) >> 6;
+  uint4 v[4];
+  auto fetch = [&](int slab) {
+    const int c = slab * 64 + chunk * 8;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      v[i] = row[i] >= 0 && c < C ? *reinterpret_cast<const uint4*>(src + (int64_t)row[i] * C + c)
+                                  : make_uint4(0, 0, 0, 0);
+  };
+  int slab = blockIdx.x;
+  if (slab < n_slab) fetch(slab);
   const int warp = tid >> 5, lane = tid & 31;
+  for (; slab < n_slab; slab += gridDim.x) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint16_t* e = reinterpret_cast<const uint16_t*>(&v[i]);
+      const int cl = (tid >> 3) + 32 * i;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) tile[chunk * 8 + j][cl] = e[j];
+    }
+    __syncthreads();
+    if (slab + (int)gridDim.x < n_slab) fetch(slab + gridDim.x);
+    const int c0 = slab * 64;
+    if constexpr (FQ) {
+      // four lanes per dst row (lanes r, r + 8, r + 16, r + 24 of warp w: row
+      // 8 w + r), lane quarter q holding columns 32 m + 8 q .. + 7 (m = 0..3):
+      // the block's scale is computed once per 32 values, and each store is a
+      // 16-byte piece of 64 contiguous bytes per row
+      const int r = lane & 7, q = lane >> 3, cl = 8 * warp + r, c = c0 + cl;
+      const uint16_t* row = &tile[cl][8 * q];  // + 32 m + 2 i: columns 32 m + 8 q + 2 i, + 1
+      // amax (a first pass over the row): with the sign bits cleared, bf16
+      // patterns order as their values
+      uint32_t mx = 0;
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          mx = __vmaxu2(mx, *reinterpret_cast<const uint32_t*>(row + 32 * m + 2 * i) & 0x7FFF7FFFu);
+      mx = max(mx & 0xFFFFu, mx >> 16);
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float amax = __uint_as_float(mx << 16);
+      float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+      if (pow2) scale = pow2_ceil(scale);
+      const float inv = 1.0f / scale;
+      __nv_bfloat16* o = dst + (int64_t)c * ldd;
+#pragma unroll 1
+      for (int m = 0; m < 4; ++m) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t x = *reinterpret_cast<const uint32_t*>(row + 32 * m + 2 * i);
+          const float f0 = __uint_as_float(x << 16), f1 = __uint_as_float(x & 0xFFFF0000u);
+          const __nv_fp8x2_storage_t e = __nv_cvt_float2_to_fp8x2(make_float2(f0 * inv, f1 * inv), __NV_SATFINITE,
+                                                                  __NV_E4M3);
+          const float2 back = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(e, __NV_E4M3)));
+          w[i] = pack_bf16x2(back.x * scale, back.y * scale);
+        }
+        const int col = col0 + 32 * m + 8 * q;
+        if (c >= C) continue;
+        if (col + 8 <= n_cols) {
+          *reinterpret_cast<uint4*>(o + col) = make_uint4(w[0], w[1], w[2], w[3]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int cc = col + 2 * i;
+            if (cc + 1 < n_cols) *reinterpret_cast<uint32_t*>(o + cc) = w[i];
+            else if (cc < n_cols) *reinterpret_cast<uint16_t*>(o + cc) = static_cast<uint16_t>(w[i] & 0xFFFFu);
+          }
+        }
+      }
+    } else {
 #pragma unroll 2
-  for (int i = 0; i < 8; ++i) {
-    const int cl = warp + 8 * i, c = c0 + cl;
-    float v[4], amax = 0.0f;
+      for (int i = 0; i < 8; ++i) {
+        const int cl = warp + 8 * i, c = c0 + cl;  // lane: columns 2 lane, +1 and 64 + 2 lane, +1
+        if (c >= C) continue;
+        const uint32_t w[2] = {*reinterpret_cast<const uint32_t*>(&tile[cl][2 * lane]),
+                               *reinterpret_cast<const uint32_t*>(&tile[cl][64 + 2 * lane])};
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      v[2 * j] = tile[cl][2 * lane + 64 * j];
-      v[2 * j + 1] = tile[cl][2 * lane + 1 + 64 * j];
-      amax = fmaxf(amax, fmaxf(fabsf(v[2 * j]), fabsf(v[2 * j + 1])));
+        for (int j = 0; j < 2; ++j) {
+          const int col = col0 + 2 * lane + 64 * j;
+          if (col >= n_cols) continue;
+          __nv_bfloat16* o = dst + (int64_t)c * ldd + col;
+          if (col + 1 < n_cols) *reinterpret_cast<uint32_t*>(o) = w[j];
+          else *reinterpret_cast<uint16_t*>(o) = static_cast<uint16_t>(w[j] & 0xFFFFu);
+        }
+      }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    if (c >= C) continue;
-    float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
-    if (pow2) scale = pow2_ceil(scale);
-    const float inv = 1.0f / scale;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int col = col0 + 2 * lane + 64 * j;
-      if (col >= n_cols) continue;
-      const __nv_fp8x2_storage_t q =
-          __nv_cvt_float2_to_fp8x2(make_float2(v[2 * j] * inv, v[2 * j + 1] * inv), __NV_SATFINITE, __NV_E4M3);
-      const float2 back = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(q, __NV_E4M3)));
-      __nv_bfloat16* o = dst + (int64_t)c * ldd + col;
-      if (col + 1 < n_cols) *reinterpret_cast<uint32_t*>(o) = pack_bf16x2(back.x * scale, back.y * scale);
-      else *o = __float2bfloat16_rn(back.x * scale);
-    }
+    __syncthreads();
   }
 }
 

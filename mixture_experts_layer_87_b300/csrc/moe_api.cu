@@ -846,33 +846,41 @@ moe_status xgemm_bf16(const void* w, int64_t w_rows, int Nw, int K, const void* 
   return launch_xgemm<Epi::BF16>(tw, tx, a, chunks * cdiv(Nw, 256), st);
 }
 
-// Transposed gather src [batch][rows][C] -> dst [batch][C][n_cols] (row ldd):
-// dst column col holds src row row_of_col[col] (-1: zeros), or row col while
-// col < rows when row_of_col is null.
-moe_status transpose_bf16(const void* src, int rows, int C, int64_t src_batch, const int32_t* row_of_col,
-                          int64_t n_cols, void* dst, int64_t ldd, int64_t dst_batch, int batch, cudaStream_t st) {
+// Transposed gather src [batch][rows][C] -> dst [batch][C][n_cols] (row ldd)
+// of transpose_cols_kernel: dst column col holds src row row_of_col[col]
+// (through perm when given; -1: zeros), or row col while col < rows when
+// row_of_col is null; with n_live (a device count) only the columns below it.
+// FQ: the FP8 weight-gradient operands, quantised 1 x 128 along the columns
+// and dequantised to bf16.
+template <bool FQ>
+moe_status transpose_cols(const void* src, int rows, int C, int64_t src_batch, const int32_t* row_of_col,
+                          const int32_t* perm, const int32_t* n_live, int64_t n_cols, void* dst, int64_t ldd,
+                          int64_t dst_batch, int batch, bool pow2, cudaStream_t st) {
   if (n_cols <= 0 || C <= 0 || batch <= 0) return MOE_OK;
-  if (C % 8 || ldd % 2 || n_cols > INT_MAX) return MOE_ERR_UNSUPPORTED;
-  dim3 grid(static_cast<unsigned>(cdiv(C, 64)), static_cast<unsigned>(cdiv(n_cols, 64)), static_cast<unsigned>(batch));
-  transpose_bf16_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, C, src_batch, row_of_col,
-                                               static_cast<int>(n_cols), static_cast<__nv_bfloat16*>(dst), ldd,
-                                               dst_batch);
+  if (C % 8 || ldd % (FQ ? 8 : 2) || n_cols > INT_MAX || (reinterpret_cast<uintptr_t>(dst) & (FQ ? 15 : 3)))
+    return MOE_ERR_UNSUPPORTED;
+  // enough blocks for ~16 per SM; each walks n_slab / split slabs of 64 c
+  const int64_t col_tiles = cdiv(n_cols, 128) * batch, n_slab = cdiv(C, 64);
+  const int64_t split = std::min<int64_t>(n_slab, std::max<int64_t>(1, cdiv(int64_t(148) * 16, col_tiles)));
+  dim3 grid(static_cast<unsigned>(split), static_cast<unsigned>(cdiv(n_cols, 128)), static_cast<unsigned>(batch));
+  transpose_cols_kernel<FQ><<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, C, src_batch,
+                                                  row_of_col, perm, static_cast<int>(n_cols), n_live,
+                                                  static_cast<__nv_bfloat16*>(dst), ldd, dst_batch, pow2);
   return launched();
 }
 
-// The FP8 weight-gradient operands: transposed gather with 1 x 128
-// quantisation along the tokens, dequantised to bf16 (transpose_fq_kernel);
-// perm (optional) maps the gathered row once more (the routed experts' u rows).
+moe_status transpose_bf16(const void* src, int rows, int C, int64_t src_batch, const int32_t* row_of_col,
+                          const int32_t* n_live, int64_t n_cols, void* dst, int64_t ldd, int64_t dst_batch, int batch,
+                          cudaStream_t st) {
+  return transpose_cols<false>(src, rows, C, src_batch, row_of_col, nullptr, n_live, n_cols, dst, ldd, dst_batch,
+                               batch, false, st);
+}
+
 moe_status transpose_fq(const void* src, int rows, int C, int64_t src_batch, const int32_t* row_of_col,
-                        const int32_t* perm, int64_t n_cols, void* dst, int64_t ldd, int64_t dst_batch, int batch,
-                        bool pow2, cudaStream_t st) {
-  if (n_cols <= 0 || C <= 0 || batch <= 0) return MOE_OK;
-  if (C % 8 || n_cols > INT_MAX) return MOE_ERR_UNSUPPORTED;
-  dim3 grid(static_cast<unsigned>(cdiv(C, 64)), static_cast<unsigned>(cdiv(n_cols, 128)), static_cast<unsigned>(batch));
-  transpose_fq_kernel<<<grid, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(src), rows, C, src_batch, row_of_col,
-                                             perm, static_cast<int>(n_cols), static_cast<__nv_bfloat16*>(dst), ldd,
-                                             dst_batch, pow2);
-  return launched();
+                        const int32_t* perm, const int32_t* n_live, int64_t n_cols, void* dst, int64_t ldd,
+                        int64_t dst_batch, int batch, bool pow2, cudaStream_t st) {
+  return transpose_cols<true>(src, rows, C, src_batch, row_of_col, perm, n_live, n_cols, dst, ldd, dst_batch, batch,
+                              pow2, st);
 }
 
 // 1 x 128 quantisation of bf16 rows [rows, C] -> codes + scales [C/128][scale_ld].
@@ -1080,13 +1088,14 @@ moe_status backward_fp8(const moe_dims& d, const BwdLayout& B, const moe_weights
   void* dyT = at<void>(ws, B.dyT);
   void* hT = at<void>(ws, B.hT);
   void* dabT = at<void>(ws, B.dabT);
-  MOE_TRY(transpose_fq(u, Ti, static_cast<int>(D), 0, row_of_col, perm, B.Rp, xT, B.Rp, 0, 1, pow2, st));
-  MOE_TRY(transpose_fq(dy, static_cast<int>(R), static_cast<int>(D), 0, row_of_col, nullptr, B.Rp, dyT, B.Rp, 0, 1,
+  const int32_t* live = pad_off + Ei;  // padded total: the columns the weight-gradient GEMM reads
+  MOE_TRY(transpose_fq(u, Ti, static_cast<int>(D), 0, row_of_col, perm, live, B.Rp, xT, B.Rp, 0, 1, pow2, st));
+  MOE_TRY(transpose_fq(dy, static_cast<int>(R), static_cast<int>(D), 0, row_of_col, nullptr, live, B.Rp, dyT, B.Rp,
+                       0, 1, pow2, st));
+  MOE_TRY(transpose_fq(hb, static_cast<int>(R), static_cast<int>(I), 0, row_of_col, nullptr, live, B.Rp, hT, B.Rp, 0, 1,
                        pow2, st));
-  MOE_TRY(transpose_fq(hb, static_cast<int>(R), static_cast<int>(I), 0, row_of_col, nullptr, B.Rp, hT, B.Rp, 0, 1,
-                       pow2, st));
-  MOE_TRY(transpose_fq(dab, static_cast<int>(R), static_cast<int>(I2), 0, row_of_col, nullptr, B.Rp, dabT, B.Rp, 0,
-                       1, pow2, st));
+  MOE_TRY(transpose_fq(dab, static_cast<int>(R), static_cast<int>(I2), 0, row_of_col, nullptr, live, B.Rp, dabT,
+                       B.Rp, 0, 1, pow2, st));
   MOE_TRY(wgrad(dyT, B.Rp, static_cast<int>(D), hT, B.Rp, static_cast<int>(I), wg_r, Ei, gr->dw2, queue + 8, status,
                 st));
   MOE_TRY(wgrad(dabT, B.Rp, static_cast<int>(I2), xT, B.Rp, static_cast<int>(D), wg_r, Ei, gr->dw13, queue + 9,
@@ -1097,11 +1106,12 @@ moe_status backward_fp8(const moe_dims& d, const BwdLayout& B, const moe_weights
     void* hsT = at<void>(ws, B.hsT);
     void* dabsT = at<void>(ws, B.dabsT);
     const int Tp = static_cast<int>(B.Tp);
-    MOE_TRY(transpose_fq(u, Ti, static_cast<int>(D), 0, nullptr, nullptr, Tp, uT, Tp, 0, 1, pow2, st));
-    MOE_TRY(transpose_fq(dout, Ti, static_cast<int>(D), 0, nullptr, nullptr, Tp, GT, Tp, 0, 1, pow2, st));
-    MOE_TRY(transpose_fq(hsb, Ti, static_cast<int>(I), T * I, nullptr, nullptr, Tp, hsT, Ns * Tp, Tp, Nsi, pow2, st));
-    MOE_TRY(transpose_fq(dab_s, Ti, static_cast<int>(I2), T * I2, nullptr, nullptr, Tp, dabsT, Ns * Tp, Tp, Nsi, pow2,
-                         st));
+    MOE_TRY(transpose_fq(u, Ti, static_cast<int>(D), 0, nullptr, nullptr, nullptr, Tp, uT, Tp, 0, 1, pow2, st));
+    MOE_TRY(transpose_fq(dout, Ti, static_cast<int>(D), 0, nullptr, nullptr, nullptr, Tp, GT, Tp, 0, 1, pow2, st));
+    MOE_TRY(transpose_fq(hsb, Ti, static_cast<int>(I), T * I, nullptr, nullptr, nullptr, Tp, hsT, Ns * Tp, Tp, Nsi,
+                         pow2, st));
+    MOE_TRY(transpose_fq(dab_s, Ti, static_cast<int>(I2), T * I2, nullptr, nullptr, nullptr, Tp, dabsT, Ns * Tp, Tp,
+                         Nsi, pow2, st));
     WgradGroup* wg_s2 = at<WgradGroup>(ws, B.wg_s2);
     WgradGroup* wg_s13 = at<WgradGroup>(ws, B.wg_s13);
     wgrad_strided_table_kernel<<<1, 256, 0, st>>>(Nsi, 0, Tp, Tp, wg_s2);   // A = G^T, B = h_s^T
@@ -1176,8 +1186,9 @@ moe_status moe_transpose_expert_weights(int32_t n_experts, int32_t inter, int32_
   if (!w13 || !w2 || !w13t || !w2t) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t I2 = 2 * int64_t(inter);
-  MOE_TRY(transpose_bf16(w13, static_cast<int>(I2), d, I2 * d, nullptr, I2, w13t, I2, I2 * d, n_experts, st));
-  return transpose_bf16(w2, d, inter, int64_t(d) * inter, nullptr, d, w2t, d, int64_t(d) * inter, n_experts, st);
+  MOE_TRY(
+      transpose_bf16(w13, static_cast<int>(I2), d, I2 * d, nullptr, nullptr, I2, w13t, I2, I2 * d, n_experts, st));
+  return transpose_bf16(w2, d, inter, int64_t(d) * inter, nullptr, nullptr, d, w2t, d, int64_t(d) * inter, n_experts, st);
 }
 
 moe_status moe_transpose_expert_weights_fp8(int32_t n_experts, int32_t inter, int32_t d, const uint8_t* w13,
@@ -1342,10 +1353,12 @@ moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_we
   void* hT = at<void>(ws, B.hT);
   void* dabT = at<void>(ws, B.dabT);
   // the padding columns are written as zeros by the transposes themselves
-  MOE_TRY(transpose_bf16(x, static_cast<int>(R), static_cast<int>(D), 0, row_of_col, B.Rp, xT, B.Rp, 0, 1, st));
-  MOE_TRY(transpose_bf16(dy, static_cast<int>(R), static_cast<int>(D), 0, row_of_col, B.Rp, dyT, B.Rp, 0, 1, st));
-  MOE_TRY(transpose_bf16(h, static_cast<int>(R), static_cast<int>(I), 0, row_of_col, B.Rp, hT, B.Rp, 0, 1, st));
-  MOE_TRY(transpose_bf16(dab, static_cast<int>(R), static_cast<int>(I2), 0, row_of_col, B.Rp, dabT, B.Rp, 0, 1, st));
+  const int32_t* live = pad_off + E;  // padded total: the columns the weight-gradient GEMM reads
+  MOE_TRY(transpose_bf16(x, static_cast<int>(R), static_cast<int>(D), 0, row_of_col, live, B.Rp, xT, B.Rp, 0, 1, st));
+  MOE_TRY(transpose_bf16(dy, static_cast<int>(R), static_cast<int>(D), 0, row_of_col, live, B.Rp, dyT, B.Rp, 0, 1, st));
+  MOE_TRY(transpose_bf16(h, static_cast<int>(R), static_cast<int>(I), 0, row_of_col, live, B.Rp, hT, B.Rp, 0, 1, st));
+  MOE_TRY(
+      transpose_bf16(dab, static_cast<int>(R), static_cast<int>(I2), 0, row_of_col, live, B.Rp, dabT, B.Rp, 0, 1, st));
   MOE_TRY(wgrad(dyT, B.Rp, static_cast<int>(D), hT, B.Rp, static_cast<int>(I), wg_r, static_cast<int>(E), gr->dw2,
                 queue + 8, status, st));
   MOE_TRY(wgrad(dabT, B.Rp, static_cast<int>(I2), xT, B.Rp, static_cast<int>(D), wg_r, static_cast<int>(E), gr->dw13,
@@ -1357,10 +1370,10 @@ moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_we
     void* hsT = at<void>(ws, B.hsT);
     void* dabsT = at<void>(ws, B.dabsT);
     const int Tp = static_cast<int>(B.Tp), Ti = static_cast<int>(T), Nsi = static_cast<int>(Ns);
-    MOE_TRY(transpose_bf16(u, Ti, static_cast<int>(D), 0, nullptr, Tp, uT, Tp, 0, 1, st));
-    MOE_TRY(transpose_bf16(dout, Ti, static_cast<int>(D), 0, nullptr, Tp, GT, Tp, 0, 1, st));
-    MOE_TRY(transpose_bf16(h_s, Ti, static_cast<int>(I), T * I, nullptr, Tp, hsT, Ns * Tp, Tp, Nsi, st));
-    MOE_TRY(transpose_bf16(dab_s, Ti, static_cast<int>(I2), T * I2, nullptr, Tp, dabsT, Ns * Tp, Tp, Nsi, st));
+    MOE_TRY(transpose_bf16(u, Ti, static_cast<int>(D), 0, nullptr, nullptr, Tp, uT, Tp, 0, 1, st));
+    MOE_TRY(transpose_bf16(dout, Ti, static_cast<int>(D), 0, nullptr, nullptr, Tp, GT, Tp, 0, 1, st));
+    MOE_TRY(transpose_bf16(h_s, Ti, static_cast<int>(I), T * I, nullptr, nullptr, Tp, hsT, Ns * Tp, Tp, Nsi, st));
+    MOE_TRY(transpose_bf16(dab_s, Ti, static_cast<int>(I2), T * I2, nullptr, nullptr, Tp, dabsT, Ns * Tp, Tp, Nsi, st));
     WgradGroup* wg_s2 = at<WgradGroup>(ws, B.wg_s2);
     WgradGroup* wg_s13 = at<WgradGroup>(ws, B.wg_s13);
     wgrad_strided_table_kernel<<<1, 256, 0, st>>>(Nsi, 0, Tp, Tp, wg_s2);       // A = G^T, B = h_s^T
