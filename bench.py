@@ -25,6 +25,7 @@ import statistics
 import subprocess
 import sys
 import time
+from dataclasses import replace
 
 import numpy as np
 import torch
@@ -635,6 +636,8 @@ def main():
     ap.add_argument("--no-variants", action="store_true", help="skip the mid, FP8 and decode measurements")
     ap.add_argument("--prec", default=None, choices=["bf16", "fp8", "fp8_ue8m0"],
                     help="override the workload's precision")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the workload's token count T (its name gets a _T<n> suffix; no variants)")
     ap.add_argument("--cpu-tokens", type=int, default=512, help="tokens in the CPU-oracle baseline sample")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--ref-tokens", type=int, default=0,
@@ -684,7 +687,7 @@ def main():
                               "data": "synthetic", "config": {"workload": "decode"}, "clocks": clk, "decode": dec}))
         return
 
-    cfg = synth.get_config(args.workload)
+    cfg = layer_config(args)
     clocks.start()
     res = measure(cfg, args, world, pk)
     clk = clocks.stop()
@@ -694,7 +697,7 @@ def main():
     launches_per_step = 8 + (2 if cfg.n_shared else 0)
 
     variants = {}
-    if not args.no_variants and args.workload == "v3":
+    if not args.no_variants and args.workload == "v3" and not args.tokens:
         variants["v3_replicated"] = measure_replicated(layer, cfg, res, args, world)
         variants["v3_backward"] = measure_backward(layer, cfg, res["u_host"].cuda(), res["bias"], pk)
         del layer, res["layer"]
@@ -755,6 +758,19 @@ def main():
         print(json.dumps(line), flush=True)
 
 
+def layer_config(args):
+    """The workload's config with the --prec / --tokens overrides; a token
+    override renames it, so no figure recorded for the named size (profiled
+    DRAM traffic) is applied to another size."""
+    over = {}
+    if args.prec:
+        over["prec"] = args.prec
+    if args.tokens:
+        over["T"] = args.tokens
+    cfg = synth.get_config(args.workload, **over)
+    return replace(cfg, name=f"{cfg.name}_T{args.tokens}") if args.tokens else cfg
+
+
 def profile_case(args):
     """The program ncu wraps: build the workload's layer, run warmup + steps
     forwards (launch order per forward: router GEMM, top-k, scan, plan,
@@ -762,7 +778,7 @@ def profile_case(args):
     down GEMM, combine) -- or, with --backward, backward passes (after the
     untimed weight transposes) --, check the device status, exit."""
     torch.cuda.set_device(0)
-    cfg = synth.get_config(args.workload, **({"prec": args.prec} if args.prec else {}))
+    cfg = layer_config(args)
     layer = build_layer(cfg)
     u = synth.tokens(cfg).cuda()
     bias = synth.bias(cfg).cuda()
