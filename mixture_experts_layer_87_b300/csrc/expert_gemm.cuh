@@ -19,13 +19,14 @@
 // dynamically (the item ring below), so SMs that drew cheap items (short
 // chunks) take more of them.  The shared-memory ring and the TMEM buffers
 // carry on from one item to the next, so the loads of the next item overlap
-// the epilogue of the current one.
+// the epilogue of the current one.  Two shapes (XShape): narrow, CH = 128
+// tokens with two TMEM buffers of 2 x 128 columns (the epilogue of item i
+// overlaps the MMAs of item i + 1); wide, CH = 256 with one buffer of
+// 2 x 256 columns and one weight stage feeding twice the MMAs.
 //
 // Warp roles: warp 0 issues the TMA loads, one thread of warp 1 issues the
 // MMAs (kind::f16, K = 16; warp 1 also owns the TMEM allocation), warps 2..9
-// drain the accumulators (two TMEM buffers of 2 x 128 columns, so the
-// epilogue of item i overlaps the MMAs of item i + 1), warp 10 fetches and
-// decodes the items.
+// drain the accumulators, warp 10 fetches and decodes the items.
 //
 // Epilogues: BF16 stores y as bf16; SWIGLU pairs gate feature f (half 0) with
 // up feature f (half 1) -- the w13 interleave puts both in one weight block --
@@ -140,25 +141,40 @@ __device__ __forceinline__ bool ring_put(const ItemRing& r, uint32_t lt, const i
 }
 
 // ---------------------------------------------------------------------------
-constexpr int kXChunk = 128;   // token rows per chunk (the N of one MMA at most)
-constexpr int kXStages = 4;
+constexpr int kXChunk = 128;   // token rows per chunk of the group tables (plan_kernel)
 constexpr int kXEpiWarps = 8;
 constexpr int kXThreads = 32 * (3 + kXEpiWarps);
 constexpr uint32_t kXABytes = 256 * 128;      // weight tile per stage (256 rows x 128 bytes of K)
-constexpr uint32_t kXBBytes = kXChunk * 128;  // token tile per stage
 
+// Two shapes of the kernel.  Narrow: an item is one chunk of <= 128 tokens,
+// 4 operand stages, two TMEM accumulator buffers (the epilogue of an item
+// overlaps the MMAs of the next).  Wide: an item is two consecutive chunks
+// of a group (<= 256 tokens, N up to 256), so each weight stage feeds twice
+// the MMA work; 3 stages of 64 KB and one TMEM buffer of 2 x 256 columns.
+// Which is faster depends on the GEMM (measured per launch site).
+template <bool WIDE>
+struct XShape {
+  static constexpr int CH = WIDE ? 2 * kXChunk : kXChunk;  // token rows per item
+  static constexpr int STAGES = WIDE ? 3 : 4;
+  static constexpr int NACC = WIDE ? 1 : 2;
+  static constexpr uint32_t B_BYTES = CH * 128;  // token tile per stage
+};
+
+template <bool WIDE>
 constexpr size_t xgemm_smem_bytes() {
-  return 1024 + size_t(kXStages) * (kXABytes + kXBBytes) + 512 /* barriers + item ring */;
+  return 1024 + size_t(XShape<WIDE>::STAGES) * (kXABytes + XShape<WIDE>::B_BYTES) + 512 /* barriers + item ring */;
 }
 
 struct XTile {
-  int32_t g, fb, c, a_row, out_row, n_valid;
+  int32_t g, fb, c, a_row, out_row, n_valid;  // n_valid 0: no work (the odd chunk of a wide pair)
 };
 
-// Items of the launch: n_groups uniform groups, or (table) *ch_total chunks,
-// each times the nb weight blocks.
+// Items of the launch: n_groups uniform groups of CH-row items, or (table)
+// *ch_total chunks, each times the nb weight blocks.
+template <bool WIDE>
 __device__ __forceinline__ int xitems(const XGemmArgs& a, int nb) {
-  if (a.groups == nullptr) return (a.uni_m + kXChunk - 1) / kXChunk * nb * a.n_groups;
+  constexpr int ch = XShape<WIDE>::CH;
+  if (a.groups == nullptr) return (a.uni_m + ch - 1) / ch * nb * a.n_groups;
   return __ldg(a.ch_total) * nb;
 }
 
@@ -167,9 +183,12 @@ __device__ __forceinline__ int xitems(const XGemmArgs& a, int nb) {
 // chunks fastest, so group g owns items [mt_start_g * nb, (mt_start_g +
 // nch_g) * nb) and chunk_group[tile / nb] names its group (low 16 bits) and
 // the expert whose weights the group uses (high 16 bits; plan_kernel fills
-// both): two dependent loads per item.
+// both): two dependent loads per item.  The wide kernel keeps the table's
+// 128-row chunks: an even chunk takes the odd one after it as well (up to
+// 256 rows), and the odd chunk's item does nothing (n_valid 0).
+template <bool WIDE>
 __device__ __forceinline__ bool xdecode(const XGemmArgs& a, int tile, int items, int nb, XTile& t) {
-  constexpr int ch = kXChunk;
+  constexpr int ch = XShape<WIDE>::CH;
   if (tile >= items) return false;
   if (a.groups == nullptr) {
     const int nch = (a.uni_m + ch - 1) / ch;
@@ -185,23 +204,24 @@ __device__ __forceinline__ bool xdecode(const XGemmArgs& a, int tile, int items,
   }
   const int cg = __ldg(a.chunk_group + tile / nb);
   const int4 G = __ldg(reinterpret_cast<const int4*>(a.groups) + (cg & 0xFFFF));  // {a_row0, out_row0, m, mt_start}
-  const int nch = (G.z + ch - 1) / ch;
+  const int nch = (G.z + kXChunk - 1) / kXChunk;
   const int local = tile - G.w * nb;
   t.g = cg >> 16;  // the weights' expert
   t.fb = local / nch;
   t.c = local - t.fb * nch;
-  t.a_row = G.x + t.c * ch;
-  t.out_row = G.y + t.c * ch;
-  t.n_valid = min(ch, G.z - t.c * ch);
+  t.a_row = G.x + t.c * kXChunk;
+  t.out_row = G.y + t.c * kXChunk;
+  t.n_valid = (WIDE && (t.c & 1)) ? 0 : min(ch, G.z - t.c * kXChunk);
   return true;
 }
 
-template <Epi EPI>
+template <Epi EPI, bool WIDE>
 __global__ void __launch_bounds__(kXThreads, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                        const XGemmArgs args) {
-  constexpr int CH = kXChunk, BK = 64, STAGES = kXStages, NACC = 2;
-  constexpr uint32_t A_BYTES = kXABytes, B_BYTES = kXBBytes;
+  using S = XShape<WIDE>;
+  constexpr int CH = S::CH, BK = 64, STAGES = S::STAGES, NACC = S::NACC;
+  constexpr uint32_t A_BYTES = kXABytes, B_BYTES = S::B_BYTES;
   constexpr uint32_t BUF_COLS = 2 * CH;  // one accumulator buffer: half 0 | half 1
   constexpr uint32_t TMEM_COLS = NACC * BUF_COLS;
   static_assert(TMEM_COLS == 512, "TMEM budget");
@@ -255,12 +275,15 @@ __global__ void __launch_bounds__(kXThreads, 1)
   if (warp == 10) {
     // ------------------------------------------------------------ item scheduler
     if (lane == 0) {
-      const int items = xitems(args, nb);
+      const int items = xitems<WIDE>(args, nb);
       int item = blockIdx.x;
       for (uint32_t lt = 0;; ++lt) {
         XTile t{-1, 0, 0, 0, 0, 0};
-        const bool have = xdecode(args, item, items, nb, t);
-        if (have) item = gridDim.x + atomicAdd(args.queue, 1);  // the next one, while this one is published
+        bool have;
+        do {  // items with nothing to do (wide: odd chunks) are passed over
+          have = xdecode<WIDE>(args, item, items, nb, t);
+          if (have) item = gridDim.x + atomicAdd(args.queue, 1);  // the next one, while this one is published
+        } while (have && t.n_valid <= 0);
         const int v[6] = {have ? t.g : -1, t.fb, t.c, t.a_row, t.out_row, t.n_valid};
         if (!ring_put(ring, lt, v, args.status, abort_flag) || !have) break;
       }

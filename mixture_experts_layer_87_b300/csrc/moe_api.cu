@@ -297,15 +297,15 @@ moe_status sm_count(int* n) {
   return MOE_OK;
 }
 
-template <Epi EPI>
+template <Epi EPI, bool WIDE>
 moe_status launch_xgemm(const CUtensorMap& tw, const CUtensorMap& tx, const XGemmArgs& a, int64_t items_bound,
                         cudaStream_t st) {
   if (items_bound <= 0) return MOE_OK;
   int sms = 0;
   MOE_TRY(sm_count(&sms));
   const int64_t grid = items_bound < sms ? items_bound : sms;
-  constexpr size_t smem = xgemm_smem_bytes();
-  auto kern = expert_gemm_kernel<EPI>;
+  constexpr size_t smem = xgemm_smem_bytes<WIDE>();
+  auto kern = expert_gemm_kernel<EPI, WIDE>;
   MOE_TRY(cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem))));
   kern<<<static_cast<unsigned>(grid), kXThreads, smem, st>>>(tw, tx, a);
   return launched();
@@ -438,15 +438,22 @@ moe_status enqueue_ffn(const moe_dims& d, const FfnOperands& o, int n_groups, co
   if (is_fp8(d))
     return enqueue_ffn_fp8(d, o, n_groups, table, ch_total, cgroup, uni_m, queue, status, st, rec);
   const int I = d.inter, D = d.d;
-  constexpr int CH = kChunkBf16;
+  // Kernel shapes (XShape), measured at V3 size: the routed gate/up GEMM runs
+  // narrow, the routed down GEMM and both GEMMs of the shared experts (every
+  // token: many chunks per weight block) run wide.
+  const bool up_wide = table == nullptr;
+  constexpr int CH_N = XShape<false>::CH, CH_W = XShape<true>::CH;
   CUtensorMap tx1, tw1, tx2, tw2;
-  MOE_TRY(make_tmap(&tx1, o.x, false, o.x_rows, D, CH));
+  MOE_TRY(make_tmap(&tx1, o.x, false, o.x_rows, D, up_wide ? CH_W : CH_N));
   MOE_TRY(make_tmap(&tw1, o.w13, false, weight_experts(o, n_groups) * 2 * I, D, 256));
-  MOE_TRY(make_tmap(&tx2, o.h, false, o.rows_cap, I, CH));
+  MOE_TRY(make_tmap(&tx2, o.h, false, o.rows_cap, I, CH_W));
   MOE_TRY(make_tmap(&tw2, o.w2, false, weight_experts(o, n_groups) * D, I, 256));
-  // upper bound of the token chunks: every group adds at most one partial chunk
-  const int64_t chunks = table ? cdiv(o.rows_cap + int64_t(CH - 1) * n_groups, CH)
-                               : int64_t(n_groups) * cdiv(uni_m, CH);
+  // upper bound of the items per weight block: a table's 128-row chunks (every
+  // group adds at most one partial chunk; the wide kernel walks the same
+  // table), or the uniform groups' items of the launch's shape
+  const int64_t table_chunks = cdiv(o.rows_cap + int64_t(kChunkBf16 - 1) * n_groups, kChunkBf16);
+  const int64_t items_up = table ? table_chunks : int64_t(n_groups) * cdiv(uni_m, up_wide ? CH_W : CH_N);
+  const int64_t items_down = table ? table_chunks : int64_t(n_groups) * cdiv(uni_m, CH_W);
 
   XGemmArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -468,7 +475,8 @@ moe_status enqueue_ffn(const moe_dims& d, const FfnOperands& o, int n_groups, co
   a.w_rows = weight_experts(o, n_groups) * 2 * I;
   a.out_rows = static_cast<int32_t>(o.rows_cap);
 #endif
-  MOE_TRY((launch_xgemm<Epi::SWIGLU>(tw1, tx1, a, chunks * cdiv(2 * I, 256), st)));
+  if (up_wide) MOE_TRY((launch_xgemm<Epi::SWIGLU, true>(tw1, tx1, a, items_up * cdiv(2 * I, 256), st)));
+  else MOE_TRY((launch_xgemm<Epi::SWIGLU, false>(tw1, tx1, a, items_up * cdiv(2 * I, 256), st)));
   if (rec) MOE_TRY(rec->mark());
 
   XGemmArgs b = a;
@@ -482,7 +490,7 @@ moe_status enqueue_ffn(const moe_dims& d, const FfnOperands& o, int n_groups, co
 #ifdef MOE_CHECK
   b.w_rows = weight_experts(o, n_groups) * D;
 #endif
-  MOE_TRY((launch_xgemm<Epi::BF16>(tw2, tx2, b, chunks * cdiv(D, 256), st)));
+  MOE_TRY((launch_xgemm<Epi::BF16, true>(tw2, tx2, b, items_down * cdiv(D, 256), st)));
   return rec ? rec->mark() : MOE_OK;
 }
 
@@ -811,17 +819,18 @@ __global__ void wgrad_strided_table_kernel(int G, int a_step, int b_step, int le
   if (g < G) out[g] = WgradGroup{g * a_step, g * b_step, len, 0};
 }
 
-// One bf16 expert-GEMM launch (BF16 epilogue): out[rows of group g] = X[rows] . W_g^T.
+// One bf16 expert-GEMM launch (BF16 epilogue): out[rows of group g] = X[rows] . W_g^T,
+// on the narrow or the wide kernel shape (XShape).
 //   table != nullptr: groups from the device table (chunk totals in mt_total,
 //   chunk -> group in cgroup); else n_groups uniform groups of uni_m rows,
 //   X rows of group g starting at g * uni_a_step, output rows at g * uni_m.
 moe_status xgemm_bf16(const void* w, int64_t w_rows, int Nw, int K, const void* x, int64_t x_rows, void* out,
                       int64_t out_ld, int n_groups, const GroupEntry* table, const int32_t* mt_total,
                       const int32_t* cgroup, int64_t chunks_bound, int uni_m, int uni_a_step, int* queue, int* status,
-                      cudaStream_t st) {
+                      bool wide, cudaStream_t st) {
   CUtensorMap tw, tx;
   MOE_TRY(make_tmap(&tw, w, false, w_rows, K, 256));
-  MOE_TRY(make_tmap(&tx, x, false, x_rows, K, kChunkBf16));
+  MOE_TRY(make_tmap(&tx, x, false, x_rows, K, wide ? XShape<true>::CH : XShape<false>::CH));
   XGemmArgs a;
   std::memset(&a, 0, sizeof(a));
   a.status = status;
@@ -842,8 +851,10 @@ moe_status xgemm_bf16(const void* w, int64_t w_rows, int Nw, int K, const void* 
   a.w_rows = w_rows;
   a.out_rows = static_cast<int32_t>(table ? x_rows : int64_t(uni_m) * n_groups);
 #endif
-  const int64_t chunks = table ? chunks_bound : int64_t(n_groups) * cdiv(uni_m, kChunkBf16);
-  return launch_xgemm<Epi::BF16>(tw, tx, a, chunks * cdiv(Nw, 256), st);
+  const int64_t chunks =
+      table ? chunks_bound : int64_t(n_groups) * cdiv(uni_m, wide ? XShape<true>::CH : XShape<false>::CH);
+  if (wide) return launch_xgemm<Epi::BF16, true>(tw, tx, a, chunks * cdiv(Nw, 256), st);
+  return launch_xgemm<Epi::BF16, false>(tw, tx, a, chunks * cdiv(Nw, 256), st);
 }
 
 // Transposed gather src [batch][rows][C] -> dst [batch][C][n_cols] (row ldd)
@@ -1271,6 +1282,8 @@ moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_we
   MOE_TRY(enqueue_dispatch(d, idx, u, mask, at<int32_t>(ws, L.wprefix), at<int32_t>(ws, L.cnt), offsets, groups,
                            mt_total, cgroup, perm, slot, x, nullptr, nullptr, nullptr, status, st));
   const int64_t chunks = cdiv(R + int64_t(kChunkBf16 - 1) * E, kChunkBf16);
+  // kernel shapes (XShape) of the backward's GEMMs, measured at V3 size
+  constexpr bool kWideAB = false, kWideDh = false, kWideDx = false, kWideShared = true;
   void* ab = at<void>(ws, B.ab);
   void* h = at<void>(ws, L.h);
   void* y = at<void>(ws, L.y);
@@ -1278,7 +1291,7 @@ moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_we
   // outputs y are not recomputed: the gates' gradient G . y is (dh . h) / g
   // (gate_grad_kernel), from dh below.
   MOE_TRY(xgemm_bf16(w->w13, E * I2, static_cast<int>(I2), static_cast<int>(D), x, R, ab, I2, static_cast<int>(E),
-                     groups, mt_total, cgroup, chunks, 0, 0, queue + 0, status, st));
+                     groups, mt_total, cgroup, chunks, 0, 0, queue + 0, status, kWideAB, st));
   swiglu_fwd_kernel<<<ew_blocks(R * I / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab), R, static_cast<int>(I),
                                                        static_cast<__nv_bfloat16*>(h));
   MOE_TRY(launched());
@@ -1293,7 +1306,7 @@ moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_we
   void* dab = at<void>(ws, B.dab);
   void* dx = at<void>(ws, B.dx);
   MOE_TRY(xgemm_bf16(wt->w2t, E * I, static_cast<int>(I), static_cast<int>(D), dy, R, dh, I, static_cast<int>(E), groups,
-                     mt_total, cgroup, chunks, 0, 0, queue + 2, status, st));
+                     mt_total, cgroup, chunks, 0, 0, queue + 2, status, kWideDh, st));
   // --- gates backward: dz, du = G + router share
   const LogitsSplit sp = logits_split(d);
   gate_grad_kernel<<<static_cast<unsigned>(T), 128, 0, st>>>(
@@ -1307,7 +1320,7 @@ moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_we
                                                        static_cast<__nv_bfloat16*>(dab));
   MOE_TRY(launched());
   MOE_TRY(xgemm_bf16(wt->w13t, E * D, static_cast<int>(D), static_cast<int>(I2), dab, R, dx, D, static_cast<int>(E),
-                     groups, mt_total, cgroup, chunks, 0, 0, queue + 3, status, st));
+                     groups, mt_total, cgroup, chunks, 0, 0, queue + 3, status, kWideDx, st));
   // --- shared experts: every token, the output gradient is G itself
   void* ab_s = at<void>(ws, B.ab_s);
   void* h_s = at<void>(ws, L.hsh);
@@ -1317,18 +1330,18 @@ moe_status moe_backward(const moe_dims* dims, const moe_weights* w, const moe_we
   if (Ns > 0) {
     const int Ti = static_cast<int>(T), Nsi = static_cast<int>(Ns);
     MOE_TRY(xgemm_bf16(w->ws13, Ns * I2, static_cast<int>(I2), static_cast<int>(D), u, T, ab_s, I2, Nsi, nullptr,
-                       nullptr, nullptr, 0, Ti, 0, queue + 4, status, st));
+                       nullptr, nullptr, 0, Ti, 0, queue + 4, status, kWideShared, st));
     swiglu_fwd_kernel<<<ew_blocks(Ns * T * I / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab_s), Ns * T,
                                                               static_cast<int>(I), static_cast<__nv_bfloat16*>(h_s));
     MOE_TRY(launched());
     MOE_TRY(xgemm_bf16(wt->ws2t, Ns * I, static_cast<int>(I), static_cast<int>(D), dout, T, dh_s, I, Nsi, nullptr,
-                       nullptr, nullptr, 0, Ti, 0, queue + 5, status, st));
+                       nullptr, nullptr, 0, Ti, 0, queue + 5, status, kWideShared, st));
     swiglu_bwd_kernel<<<ew_blocks(Ns * T * I / 8), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(ab_s),
                                                               static_cast<const __nv_bfloat16*>(dh_s), Ns * T,
                                                               static_cast<int>(I), static_cast<__nv_bfloat16*>(dab_s));
     MOE_TRY(launched());
     MOE_TRY(xgemm_bf16(wt->ws13t, Ns * D, static_cast<int>(D), static_cast<int>(I2), dab_s, Ns * T, dx_s, D, Nsi,
-                       nullptr, nullptr, nullptr, 0, Ti, Ti, queue + 6, status, st));
+                       nullptr, nullptr, nullptr, 0, Ti, Ti, queue + 6, status, kWideShared, st));
   }
   gather_dx_kernel<<<static_cast<unsigned>(T), 128, 0, st>>>(static_cast<const __nv_bfloat16*>(dx), slot, d.k, R,
                                                               static_cast<const __nv_bfloat16*>(dx_s),
