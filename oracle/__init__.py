@@ -140,11 +140,6 @@ def dispatch_layout(idx: np.ndarray, E: int):
     return dict(counts=counts, offsets=offsets, perm=perm, slot=slot)
 
 
-def near_ties(gap: np.ndarray, eps: float = 1e-4) -> np.ndarray:
-    """Tokens whose k-th and (k+1)-th biased scores differ by less than eps."""
-    return np.nonzero(gap < eps)[0]
-
-
 # ----------------------------------------------------------------------------
 # FP8 E4M3 (ai.flicky.cc 3.3)
 def e4m3_encode(x: np.ndarray) -> np.ndarray:
