@@ -88,7 +88,7 @@ def _peak_number(v):
 
 
 def peaks(path=None):
-    """Roofline denominators: the measured peaks when MEASURED_PEAKS.json
+    """Roofline denominators: the peaks measured on this machine when MEASURED_PEAKS.json
     is present and readable, else the fallback figures (source says which).
     bf16 is the burst figure (cuBLAS timed alone, at full clocks): the expert
     GEMMs are timed one forward at a time, a few milliseconds each, not in a

@@ -1,9 +1,10 @@
-"""Host logic of bench.py that needs no GPU: the roofline denominators.
+"""Host logic of bench.py that needs no GPU: the roofline denominators, the
+workload overrides.
 
-The driver writes MEASURED_PEAKS.json (HBM copy GB/s, bf16 GEMM TFLOP/s burst
-and sustained).  bench.py must use those numbers when they are there, fall
-back to the stated figures when the file is absent, and never fail the run
-because the file has another shape than expected.
+MEASURED_PEAKS.json, written on each machine, holds the HBM copy GB/s and the
+bf16 GEMM TFLOP/s (burst and sustained).  bench.py must use those numbers when
+they are there, fall back to the stated figures when the file is absent, and
+never fail the run because the file has another shape than expected.
 """
 import json
 import os
@@ -91,3 +92,15 @@ def test_clock_sampler_without_a_gpu_id_reports_nothing():
     assert s.proc is None
     out = s.stop()
     assert out["sm_mhz"] is None and "not sampled" in out["reasons"][0]
+
+
+def test_token_override_renames_the_workload():
+    """--tokens T changes the batch and the name, so a DRAM-traffic figure
+    recorded for the named size is never reported for another size."""
+    import argparse
+    a = argparse.Namespace(workload="v3", prec=None, tokens=2048)
+    cfg = bench.layer_config(a)
+    assert (cfg.T, cfg.name, cfg.d, cfg.E) == (2048, "v3_T2048", 7168, 256)
+    assert bench.kernel_traffic("routed_gate_up", cfg.name) is None
+    b = argparse.Namespace(workload="v3", prec="fp8", tokens=0)
+    assert (bench.layer_config(b).T, bench.layer_config(b).prec, bench.layer_config(b).name) == (8192, "fp8", "v3")
