@@ -438,22 +438,27 @@ moe_status enqueue_ffn(const moe_dims& d, const FfnOperands& o, int n_groups, co
   if (is_fp8(d))
     return enqueue_ffn_fp8(d, o, n_groups, table, ch_total, cgroup, uni_m, queue, status, st, rec);
   const int I = d.inter, D = d.d;
-  // Kernel shapes (XShape), measured at V3 size: the routed gate/up GEMM runs
-  // narrow, the routed down GEMM and both GEMMs of the shared experts (every
-  // token: many chunks per weight block) run wide.
-  const bool up_wide = table == nullptr;
+  // Kernel shapes (XShape), measured: both GEMMs of the shared experts (every
+  // token: many chunks per weight block) run wide; the routed gate/up GEMM runs
+  // narrow; the routed down GEMM runs wide when the launch has many wide items
+  // per SM (V3: ~70, 3-8% faster), else narrow (mid and a 32-expert slice,
+  // under 10 per SM: the longer wide items leave a longer tail, 8-13% slower).
+  int sms = 0;
+  MOE_TRY(sm_count(&sms));
   constexpr int CH_N = XShape<false>::CH, CH_W = XShape<true>::CH;
+  const bool up_wide = table == nullptr;
+  const bool down_wide = table == nullptr || (o.rows_cap / CH_W + n_groups / 2) * cdiv(D, 256) >= int64_t(24) * sms;
   CUtensorMap tx1, tw1, tx2, tw2;
   MOE_TRY(make_tmap(&tx1, o.x, false, o.x_rows, D, up_wide ? CH_W : CH_N));
   MOE_TRY(make_tmap(&tw1, o.w13, false, weight_experts(o, n_groups) * 2 * I, D, 256));
-  MOE_TRY(make_tmap(&tx2, o.h, false, o.rows_cap, I, CH_W));
+  MOE_TRY(make_tmap(&tx2, o.h, false, o.rows_cap, I, down_wide ? CH_W : CH_N));
   MOE_TRY(make_tmap(&tw2, o.w2, false, weight_experts(o, n_groups) * D, I, 256));
   // upper bound of the items per weight block: a table's 128-row chunks (every
   // group adds at most one partial chunk; the wide kernel walks the same
   // table), or the uniform groups' items of the launch's shape
   const int64_t table_chunks = cdiv(o.rows_cap + int64_t(kChunkBf16 - 1) * n_groups, kChunkBf16);
   const int64_t items_up = table ? table_chunks : int64_t(n_groups) * cdiv(uni_m, up_wide ? CH_W : CH_N);
-  const int64_t items_down = table ? table_chunks : int64_t(n_groups) * cdiv(uni_m, CH_W);
+  const int64_t items_down = table ? table_chunks : int64_t(n_groups) * cdiv(uni_m, down_wide ? CH_W : CH_N);
 
   XGemmArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -490,7 +495,8 @@ moe_status enqueue_ffn(const moe_dims& d, const FfnOperands& o, int n_groups, co
 #ifdef MOE_CHECK
   b.w_rows = weight_experts(o, n_groups) * D;
 #endif
-  MOE_TRY((launch_xgemm<Epi::BF16, true>(tw2, tx2, b, items_down * cdiv(D, 256), st)));
+  if (down_wide) MOE_TRY((launch_xgemm<Epi::BF16, true>(tw2, tx2, b, items_down * cdiv(D, 256), st)));
+  else MOE_TRY((launch_xgemm<Epi::BF16, false>(tw2, tx2, b, items_down * cdiv(D, 256), st)));
   return rec ? rec->mark() : MOE_OK;
 }
 
