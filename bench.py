@@ -72,6 +72,8 @@ def max_over_ranks(x: float, world: int) -> float:
 # ----------------------------------------------------------------------------
 # peaks and clocks
 FALLBACK_PEAKS = dict(hbm=6400.0, bf16=1800.0, bf16_sus=1400.0)
+# B300 HBM3e nominal bandwidth, reported beside the measured copy bandwidth
+NOMINAL_HBM_GBS = 7700.0
 
 
 def _peak_number(v):
@@ -296,6 +298,7 @@ def roofline(cfg, stage_ms: dict, counts, pk, kernel="routed_gate_up"):
     return {"kernel": kernel, "bound": bound, "achieved": round(ach, 2), "peak": round(peak, 1), "unit": unit,
             "frac": round(ach / peak, 4), "traffic": kernel_traffic(kernel, cfg.name),
             "tensor_frac": round(t_f / t, 4), "hbm_frac": round(t_b / t, 4),
+            "hbm_frac_of_nominal": round(B / t / 1e9 / NOMINAL_HBM_GBS, 4),
             "tflops": round(F / t / 1e12, 1), "gbs": round(B / t / 1e9, 1),
             "algorithmic_bytes": int(B), "algorithmic_flops": int(F), "ms": round(stage_ms[kernel], 4),
             "peak_source": f"tensor: {peak_what}; HBM: copy bandwidth ({pk['source']})",
@@ -542,6 +545,7 @@ def measure_decode(args, world, pk, layer=None):
     return {"value": world * cfg.T * cfg.steps / (total * 1e-3), "ms_per_step": total / cfg.steps,
             "hbm_gbs_mean": round(float(np.mean(gbs)), 1),
             "hbm_frac_of_measured": round(float(np.mean(gbs)) / pk["hbm"], 4),
+            "hbm_frac_of_nominal": round(float(np.mean(gbs)) / NOMINAL_HBM_GBS, 4),
             "max_over_mean_load_first": round(float(c[0].max() / mean), 3),
             "max_over_mean_load_last": round(float(c[-1].max() / mean), 3),
             "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},

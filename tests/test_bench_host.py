@@ -104,3 +104,18 @@ def test_token_override_renames_the_workload():
     assert bench.kernel_traffic("routed_gate_up", cfg.name) is None
     b = argparse.Namespace(workload="v3", prec="fp8", tokens=0)
     assert (bench.layer_config(b).T, bench.layer_config(b).prec, bench.layer_config(b).name) == (8192, "fp8", "v3")
+
+
+def test_roofline_reports_both_hbm_denominators():
+    """hbm_frac divides by the measured copy bandwidth, hbm_frac_of_nominal by
+    the part's nominal 7.7 TB/s; both come from the same algorithmic bytes."""
+    import numpy as np
+    import synth
+    cfg = synth.get_config("v3")
+    counts = np.full(cfg.E, cfg.T * cfg.k // cfg.E)
+    pk = dict(bench.FALLBACK_PEAKS, source="fallback")
+    r = bench.roofline(cfg, {"routed_gate_up": 4.0}, counts, pk)
+    B = bench.stage_work(cfg, counts)["routed_gate_up"][1]
+    assert abs(r["hbm_frac"] - B / 4e-3 / 1e9 / pk["hbm"]) < 1e-4
+    assert abs(r["hbm_frac_of_nominal"] - B / 4e-3 / 1e9 / bench.NOMINAL_HBM_GBS) < 1e-4
+    assert r["hbm_frac_of_nominal"] < r["hbm_frac"]
