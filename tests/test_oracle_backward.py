@@ -321,3 +321,39 @@ def test_fp8_backward_statement_catches_planted_slips(monkeypatch, slip):
     else:
         monkeypatch.setattr(ob, "fp8_roundtrip_128x128", lambda w, pow2=False: w)
     assert _compare_fp8(run(), ref, cfg) > 1e-4
+
+
+def test_one_expert_top1_is_the_gradient_of_a_dense_swiglu():
+    """E = 1, k = 1, no shared expert: the layer is h' = u + W2 (SiLU(W1 u) * W3 u)
+    (the single gate is s / s = 1), so its backward is autograd of that plain
+    expression (torch F.silu), and the centroid gets exactly no gradient."""
+    from dataclasses import replace
+    cfg = replace(synth.get_config("tiny"), E=1, k=1, n_shared=0)
+    u, c = synth.tokens(cfg), synth.centroids(cfg)
+    w1, w3, w2 = synth.expert_weights(cfg, 0)
+    idx = np.zeros((cfg.T, 1), np.int32)
+    G = np.random.default_rng(11).standard_normal((cfg.T, cfg.d))
+    bits = lambda ws: tuple(synth.bf16_bits(w) for w in ws)
+    res = ob.layer_backward(synth.bf16_bits(u), synth.bf16_bits(c), idx, G, lambda e: bits((w1, w3, w2)),
+                            lambda s: (), 0, 1)
+    ut = u.double().requires_grad_()
+    wt = [w.double().requires_grad_() for w in (w1, w3, w2)]
+    out = ut + (F.silu(ut @ wt[0].T) * (ut @ wt[1].T)) @ wt[2].T
+    (out * torch.from_numpy(G)).sum().backward()
+    tol = lambda ref: 1e-10 * max(1.0, float(np.abs(ref).max()))
+    np.testing.assert_allclose(res["du"], ut.grad.numpy(), rtol=0, atol=tol(ut.grad.numpy()))
+    for got, w in zip(res["dw_routed"][0], wt):
+        np.testing.assert_allclose(got, w.grad.numpy(), rtol=0, atol=tol(w.grad.numpy()))
+    assert not np.any(res["dcent"])
+
+
+def test_backward_of_an_empty_batch_is_zero():
+    cfg = synth.get_config("tiny")
+    c = synth.centroids(cfg)
+    bits = lambda ws: tuple(synth.bf16_bits(w) for w in ws)
+    res = ob.layer_backward(np.zeros((0, cfg.d), np.uint16), synth.bf16_bits(c), np.zeros((0, cfg.k), np.int32),
+                            np.zeros((0, cfg.d)), lambda e: bits(synth.expert_weights(cfg, e)),
+                            lambda s: bits(synth.expert_weights(cfg, s, shared=True)), cfg.n_shared, cfg.E)
+    assert res["du"].shape == (0, cfg.d) and not np.any(res["dcent"])
+    assert not res["dw_routed"]
+    assert all(not np.any(g) for ws in res["dw_shared"] for g in ws)
