@@ -144,3 +144,20 @@ def test_backward_workspace_and_argument_errors(lib):
     assert lib.moe_transpose_expert_weights_fp8(2, 128, 128, fake, None, fake, fake, fake, fake, fake, fake,
                                                 None) == 1                                  # no scales
     assert lib.moe_transpose_expert_weights(2, 100, 128, fake, fake, fake, fake, None) == 1       # I % 128
+
+
+def test_backward_rejects_bad_gradient_pointers_and_small_workspace(lib):
+    """moe_backward validates before it enqueues anything: with tokens, du must
+    be given; every gradient must be 16-byte aligned (vector and TMA stores);
+    the workspace must be at least moe_backward_workspace_size."""
+    dm = _dims()
+    need = capi.moe_backward_workspace_size(dm)
+    fake = 1 << 20
+    w = capi.moe_weights(fake, None, fake, None, fake, None, fake, None, fake)
+    wt = capi.moe_weights_t(fake, fake, fake, fake, None, None, None, None)
+    call = lambda gr, ws_bytes=need: lib.moe_backward(ctypes.byref(dm), ctypes.byref(w), ctypes.byref(wt), fake, fake,
+                                                      fake, ctypes.byref(gr), fake, ws_bytes, None)
+    assert call(capi.moe_grads(None, fake, fake, fake, fake, fake)) == 1            # du missing, T > 0
+    assert call(capi.moe_grads(fake + 8, fake, fake, fake, fake, fake)) == 1        # du misaligned
+    assert call(capi.moe_grads(fake, fake, fake + 4, fake, fake, fake)) == 1        # dw13 misaligned
+    assert call(capi.moe_grads(fake, fake, fake, fake, fake, fake), need - 256) == 3  # workspace too small
